@@ -1,0 +1,200 @@
+/*
+ * moe.h -- C ABI of the GB300-native single-GPU Mixture-of-Experts layer
+ * forward: router -> align -> expert GEMM1 + SwiGLU -> expert GEMM2 ->
+ * weighted finalize.
+ *
+ * Pages the operations follow (cited per entry point below):
+ *   [P1] "How an MoE Model Picks Its Experts During LLM Inference"
+ *   [P2] "Mixture of Experts"
+ *   [P3] "MoE Kernels, in depth"
+ *   [P4] "How GPUs Fuse Communication and Computation During LLM Inference"
+ *
+ * Common rules
+ *   - Every pointer argument is a DEVICE pointer owned by the caller, unless
+ *     the argument says "host".  The library never allocates, frees or
+ *     synchronises; every call only enqueues kernels on `stream` (a
+ *     cudaStream_t; NULL = the legacy default stream) and returns.
+ *   - Matrices are dense, row-major, contiguous.  bf16 is IEEE bfloat16;
+ *     E4M3 is OCP FP8 e4m3 (one byte); E2M1 is OCP FP4 e2m1 packed two per
+ *     byte, low nibble first.  Block scales are UE8M0 bytes (value
+ *     2^(s-127)), one per 32 consecutive values of a row along the
+ *     contraction dimension.
+ *   - Arguments are checked on the host before anything is launched; a
+ *     violation returns MOE_ERR_ARG (bad value) or MOE_ERR_UNSUPPORTED (a
+ *     valid but unimplemented combination) and launches nothing.  T = 0 is a
+ *     valid no-op.
+ *   - Errors found on the device (an expert id outside [0,E), a bounded wait
+ *     that expired) never trap: the kernel skips the offending access and ORs
+ *     a code into the sticky error word at the start of the workspace; read
+ *     it with moe_read_device_error.
+ *   - Workspace: `ws` is caller-owned device memory of at least the size the
+ *     matching *_workspace_bytes function returns, 256-byte aligned.  It must
+ *     be zeroed once before its first use (moe_workspace_init); the library
+ *     leaves it in a reusable state after every successful call.  Two calls
+ *     that overlap in time must not share a workspace.
+ */
+#ifndef ROUTER_EXPERTS_GB300_MOE_H
+#define ROUTER_EXPERTS_GB300_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_ARG = 1,          /* invalid argument (nothing launched)              */
+  MOE_ERR_UNSUPPORTED = 2,  /* valid but unimplemented combination              */
+  MOE_ERR_CUDA = 3,         /* a CUDA runtime/driver call failed                */
+  MOE_ERR_DEVICE = 4        /* returned by moe_read_device_error when set       */
+} moe_status;
+
+typedef enum { MOE_SCORING_SOFTMAX = 0, MOE_SCORING_SIGMOID = 1 } moe_scoring;
+
+typedef enum { MOE_DT_BF16 = 0, MOE_DT_F32 = 1, MOE_DT_E4M3 = 2, MOE_DT_E2M1 = 3 } moe_dtype;
+
+/* Bits of the device error word. */
+#define MOE_DEVERR_BAD_EXPERT_ID 1 /* an expert id outside [0,E) was skipped          */
+#define MOE_DEVERR_WAIT_TIMEOUT 2  /* a bounded in-kernel wait expired; outputs invalid */
+#define MOE_DEVERR_BAD_TABLE 4     /* a block table entry was out of range (clamped)  */
+
+/* ---------------------------------------------------------------------------
+ * Router.  [P1] §1.1 (three steps: gate GEMM, scores, top-k + rescale),
+ * §1.3 (rank key = score + bias used only for selection; the weight is the
+ * unbiased score, Figure 3), §2.4 (bf16 inputs, fp32 logits and bias), §4
+ * (reference router: weights / (sum + 1e-20)), §5.3 (one warp per token row,
+ * k rounds, lowest expert id wins ties).  [P2] "Mixture of Experts", the gate
+ * (a d x E linear without bias) and DeepSeek's grouped, bias-corrected
+ * routing: group score = sum of the two largest rank keys of the group, keep
+ * topk_group groups, mask the rest, top-k, weights from the original scores,
+ * renormalise, multiply by the routed scaling factor.
+ *
+ *   hidden       [T,H] in hidden_dt: BF16, F32, or E4M3 with hidden_scale
+ *                [T,H/32] (the router then sees the exact dequantised value)
+ *   gate         [E,H] in gate_dt: BF16 or F32
+ *   bias         [E] fp32 selection bias, or NULL for none
+ *   scoring      MOE_SCORING_SOFTMAX (over all E logits) or _SIGMOID
+ *   n_group      1 = plain top-k; else E % n_group == 0, E/n_group >= 2,
+ *                1 <= topk_group <= n_group, topk_group*E/n_group >= k
+ *   renormalize  nonzero: w_j /= (sum_j w_j + 1e-20); then w_j *= scaling
+ *   topk_ids     [T,k] int32 out, selection order (best first)
+ *   topk_weights [T,k] fp32 out
+ * Limits: 1 <= k <= min(E,16), E <= 512, H % 32 == 0.  Logits are fp32 sums
+ * of exact products (fp32 inputs are split into three bf16 parts).
+ * ------------------------------------------------------------------------- */
+size_t moe_router_workspace_bytes(int T, int H, int E);
+int moe_router(const void* hidden, int hidden_dt, const uint8_t* hidden_scale, const void* gate,
+               int gate_dt, const float* bias, int T, int H, int E, int k, int scoring,
+               int n_group, int topk_group, int renormalize, float scaling, int32_t* topk_ids,
+               float* topk_weights, void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Align (moe_align_block_size).  [P3] "Alignment: making ragged routing
+ * tileable" (count per expert, round up to block_m, exclusive prefix sum,
+ * sorted assignment ids with the sentinel T*k for padding, expert of every
+ * block, padded length; no host sync; buffers sized for the worst case
+ * T*k + E*(block_m-1)).  [P2] "vLLM's Triton path: align, then index" (worked
+ * example; unused block entries are -1).
+ *
+ *   topk_ids        [T,k] int32; assignment a = t*k + j
+ *   sorted_ids      [cap_rows] int32 out: assignments grouped by expert in
+ *                   ascending expert id, within an expert in ascending a
+ *                   (deterministic); pads and the tail hold T*k
+ *   cap_rows        >= T*k + E*(block_m-1)
+ *   block_expert    [ceil(cap_rows/block_m)] int32 out; -1 past the end
+ *   num_post_padded [1] int32 out: sum over experts of ceil(count/block_m)*block_m
+ * Limits: block_m in {16, 64, 128}; E <= 1024.  An id outside [0,E) is
+ * skipped (not placed) and sets MOE_DEVERR_BAD_EXPERT_ID.
+ * ------------------------------------------------------------------------- */
+size_t moe_align_workspace_bytes(void);
+int moe_align(const int32_t* topk_ids, int T, int k, int E, int block_m, int32_t* sorted_ids,
+              int64_t cap_rows, int32_t* block_expert, int32_t* num_post_padded, void* ws,
+              size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Expert GEMMs.  [P3] "The fused expert GEMM" (each tile looks up its expert
+ * in block_expert and its rows in sorted_ids; the activation gather is folded
+ * into the operand load; padding rows masked; gate and up are one 2F x H
+ * matrix with SwiGLU silu(g) * u in the epilogue; the routing weight is
+ * applied in the down GEMM's epilogue so the combine is a plain sum).
+ * [P2] w13 [E, 2F, H] (gate rows 0..F-1, up rows F..2F-1), w2 [E, H, F].
+ * [P4] §3.5: SwiGLU and FP8 re-quantisation (a power-of-two scale per 32
+ * values, the smallest with amax/scale <= 448) fused into one epilogue.
+ *
+ * moe_expert_gemm1: inter[p, f] = silu(g) * u for every padded row p <
+ *   num_post_padded, where g/u are row (sorted_ids[p] / k) of x times the
+ *   gate/up rows of w13[block_expert[p / block_m]]; pad rows are written 0.
+ *   act_dt BF16: x [T,H] bf16, inter [cap_rows, F] bf16.
+ * moe_expert_gemm2: stage[a, h] = bf16(weight[a] * sum_f inter[p, f] * w2[e, h, f])
+ *   for every real row p (a = sorted_ids[p] < T*k).
+ * moe_grouped_ffn: both, with inter held in the workspace.
+ * w_dt must equal act_dt (BF16) or be E2M1 with act_dt E4M3 (low-bit:
+ * MOE_ERR_UNSUPPORTED until built).  Limits: H % 64 == 0, F % 32 == 0,
+ * block_m in {16, 64, 128}.
+ * ------------------------------------------------------------------------- */
+size_t moe_ffn_workspace_bytes(int T, int H, int F, int E, int k, int block_m, int act_dt);
+int moe_expert_gemm1(const void* x, int act_dt, const uint8_t* x_scale, const void* w13,
+                     const uint8_t* w13_scale, int w_dt, int T, int H, int F, int E, int k,
+                     int block_m, const int32_t* sorted_ids, const int32_t* block_expert,
+                     const int32_t* num_post_padded, int64_t cap_rows, void* inter,
+                     uint8_t* inter_scale, void* ws, size_t ws_bytes, void* stream);
+int moe_expert_gemm2(const void* inter, const uint8_t* inter_scale, int act_dt, const void* w2,
+                     const uint8_t* w2_scale, int w_dt, int T, int H, int F, int E, int k,
+                     int block_m, const int32_t* sorted_ids, const int32_t* block_expert,
+                     const int32_t* num_post_padded, int64_t cap_rows,
+                     const float* topk_weights, void* stage, void* ws, size_t ws_bytes,
+                     void* stream);
+int moe_grouped_ffn(const void* x, const uint8_t* x_scale, int act_dt, const void* w13,
+                    const uint8_t* w13_scale, const void* w2, const uint8_t* w2_scale, int w_dt,
+                    int T, int H, int F, int E, int k, int block_m, const int32_t* sorted_ids,
+                    const int32_t* block_expert, const int32_t* num_post_padded,
+                    int64_t cap_rows, const float* topk_weights, void* stage, void* ws,
+                    size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Finalize.  [P3] "Combine" (a gather per token summing its k rows in a fixed
+ * order is deterministic); [P2] ops.moe_sum reduces the top-k axis of the
+ * [T, k, H] cache; [P4] §3.7 (add the slots as 32-bit floats in slot order,
+ * round once to 16 bits).
+ *   stage [T*k, H] bf16 (weights already applied), out [T, H] bf16:
+ *   out[t, h] = bf16(sum_{j=0..k-1} stage[t*k + j, h]) summed in fp32.
+ * ------------------------------------------------------------------------- */
+int moe_finalize(const void* stage, int T, int k, int H, void* out, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * The whole layer: router, align, GEMM1 + SwiGLU, GEMM2 + weight, finalize,
+ * enqueued back to back with no host synchronisation.  block_m = 0 picks the
+ * tile height from the mean rows per expert T*k/E: 16 below 8, 64 below 64,
+ * else 128 ([P3] "Tile shape is the main tuning knob ... depends on tokens
+ * per expert").  act_dt/w_dt as for the expert GEMMs; the router reads
+ * `hidden` (dequantised when E4M3).  out [T,H] bf16.
+ * ------------------------------------------------------------------------- */
+size_t moe_layer_workspace_bytes(int T, int H, int F, int E, int k, int block_m, int act_dt);
+int moe_layer(const void* hidden, int act_dt, const uint8_t* hidden_scale, const void* gate,
+              int gate_dt, const float* bias, const void* w13, const uint8_t* w13_scale,
+              const void* w2, const uint8_t* w2_scale, int w_dt, int T, int H, int F, int E,
+              int k, int scoring, int n_group, int topk_group, int renormalize, float scaling,
+              int block_m, void* out, void* ws, size_t ws_bytes, void* stream);
+/* Tile height moe_layer uses for block_m = 0. */
+int moe_pick_block_m(int T, int k, int E);
+
+/* ---------------------------------------------------------------------------
+ * Utilities.
+ * ------------------------------------------------------------------------- */
+/* Zero `ws_bytes` bytes of a workspace (asynchronous on `stream`). */
+int moe_workspace_init(void* ws, size_t ws_bytes, void* stream);
+/* SYNCHRONISING: waits for `stream`, copies the device error word into *code
+ * (host), clears it when `clear` is nonzero.  Returns MOE_OK when the word is
+ * 0, MOE_ERR_DEVICE when it is not, MOE_ERR_CUDA on a CUDA failure. */
+int moe_read_device_error(void* ws, int32_t* code, int clear, void* stream);
+/* Human-readable status. */
+const char* moe_status_string(int status);
+/* Text of the last CUDA error seen by any entry point of this thread ("" if none). */
+const char* moe_last_cuda_error_string(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* ROUTER_EXPERTS_GB300_MOE_H */

@@ -1,0 +1,409 @@
+// api.cu -- the C ABI declared in include/moe.h: host-side argument checks,
+// workspace layout and the stream-ordered launches of the kernels.
+#include <stdio.h>
+#include <string.h>
+
+#include "../../include/moe.h"
+#include "moe_internal.h"
+
+namespace moe {
+
+static thread_local char g_last_cuda_error[256] = "";
+
+static int cuda_fail(const char* what, cudaError_t e) {
+  snprintf(g_last_cuda_error, sizeof(g_last_cuda_error), "%s: %s", what, cudaGetErrorString(e));
+  return MOE_ERR_CUDA;
+}
+static int launch_fail(const char* what) {
+  const cudaError_t e = cudaGetLastError();
+  snprintf(g_last_cuda_error, sizeof(g_last_cuda_error), "%s: %s", what,
+           e == cudaSuccess ? "launch rejected" : cudaGetErrorString(e));
+  return MOE_ERR_CUDA;
+}
+
+int device_num_sms() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (!cache[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+static bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// ---- layouts ------------------------------------------------------------------
+struct FfnLayout {
+  size_t inter, partial, total;  // offsets from the region start
+};
+static FfnLayout ffn_layout(int T, int F, int E, int k, int block_m, bool with_inter) {
+  FfnLayout L{};
+  size_t off = 0;
+  if (with_inter) {
+    const size_t cap = static_cast<size_t>(T) * k + static_cast<size_t>(E) * (block_m - 1);
+    L.inter = off;
+    off += align_up(cap * F * 2, 256);
+  }
+  L.partial = off;
+  off += ffn_partial_bytes(block_m);
+  L.total = off;
+  return L;
+}
+
+struct LayerLayout {
+  size_t ids, wts, sorted, blk, npp, stage, router, ffn, total;
+  int64_t cap;
+};
+static LayerLayout layer_layout(int T, int H, int F, int E, int k, int block_m) {
+  LayerLayout L{};
+  size_t off = kWsHeaderBytes;
+  const size_t nk = static_cast<size_t>(T) * k;
+  L.cap = static_cast<int64_t>(nk) + static_cast<int64_t>(E) * (block_m - 1);
+  L.ids = off;
+  off += align_up(nk * 4, 256);
+  L.wts = off;
+  off += align_up(nk * 4, 256);
+  L.sorted = off;
+  off += align_up(static_cast<size_t>(L.cap) * 4, 256);
+  L.blk = off;
+  off += align_up(static_cast<size_t>((L.cap + block_m - 1) / block_m) * 4, 256);
+  L.npp = off;
+  off += 256;
+  L.stage = off;
+  off += align_up(nk * H * 2, 256);
+  L.router = off;
+  off += plan_router(T, H, E).scratch_bytes;
+  L.ffn = off;
+  off += ffn_layout(T, F, E, k, block_m, true).total;
+  L.total = off;
+  return L;
+}
+
+static int* err_word(void* ws) { return reinterpret_cast<int*>(static_cast<char*>(ws) + kWsErrOffset); }
+
+// ---- checks -------------------------------------------------------------------
+static int check_router(const void* hidden, int hidden_dt, const uint8_t* hidden_scale,
+                        const void* gate, int gate_dt, int T, int H, int E, int k, int scoring,
+                        int n_group, int topk_group) {
+  if (T < 0 || H <= 0 || E <= 0 || k <= 0) return MOE_ERR_ARG;
+  if (k > E || k > 16 || E > 512 || H % 32 != 0) return MOE_ERR_ARG;
+  if (T > 16 * kRouterMaxTiles) return MOE_ERR_ARG;
+  if (scoring != MOE_SCORING_SOFTMAX && scoring != MOE_SCORING_SIGMOID) return MOE_ERR_ARG;
+  if (n_group < 1 || n_group > 32) return MOE_ERR_ARG;
+  if (n_group > 1) {
+    if (E % n_group != 0 || E / n_group < 2) return MOE_ERR_ARG;
+    if (topk_group < 1 || topk_group > n_group) return MOE_ERR_ARG;
+    if (topk_group * (E / n_group) < k) return MOE_ERR_ARG;
+  }
+  if (hidden_dt != MOE_DT_BF16 && hidden_dt != MOE_DT_F32 && hidden_dt != MOE_DT_E4M3)
+    return MOE_ERR_UNSUPPORTED;
+  if (gate_dt != MOE_DT_BF16 && gate_dt != MOE_DT_F32) return MOE_ERR_UNSUPPORTED;
+  if (T > 0) {
+    if (!hidden || !gate) return MOE_ERR_ARG;
+    if (hidden_dt == MOE_DT_E4M3 && !hidden_scale) return MOE_ERR_ARG;
+    if (!aligned(hidden, 16) || !aligned(gate, 16)) return MOE_ERR_ARG;
+  }
+  return MOE_OK;
+}
+
+static int check_block_m(int block_m) {
+  return (block_m == 16 || block_m == 64 || block_m == 128) ? MOE_OK : MOE_ERR_ARG;
+}
+
+static int check_ffn(int act_dt, int w_dt, int T, int H, int F, int E, int k, int block_m,
+                     int64_t cap_rows) {
+  if (T < 0 || H <= 0 || F <= 0 || E <= 0 || k <= 0 || k > E) return MOE_ERR_ARG;
+  if (H % 64 != 0 || F % 32 != 0) return MOE_ERR_ARG;
+  if (check_block_m(block_m) != MOE_OK) return MOE_ERR_ARG;
+  if (cap_rows < static_cast<int64_t>(T) * k + static_cast<int64_t>(E) * (block_m - 1))
+    return MOE_ERR_ARG;
+  if (cap_rows > 0x7fffffffll || static_cast<int64_t>(E) * 2 * F > 0x7fffffffll ||
+      static_cast<int64_t>(E) * H > 0x7fffffffll)
+    return MOE_ERR_ARG;
+  if (act_dt == MOE_DT_BF16 && w_dt == MOE_DT_BF16) return MOE_OK;
+  if (act_dt == MOE_DT_E4M3 && w_dt == MOE_DT_E2M1) return MOE_ERR_UNSUPPORTED;
+  return MOE_ERR_UNSUPPORTED;
+}
+
+static FfnParams ffn_params(int T, int H, int F, int E, int k, int block_m,
+                            const int32_t* sorted_ids, const int32_t* block_expert,
+                            const int32_t* npp, int64_t cap_rows, void* ws, size_t region_off,
+                            const FfnLayout& L) {
+  FfnParams p{};
+  p.sorted_ids = sorted_ids;
+  p.block_expert = block_expert;
+  p.num_post_padded = npp;
+  p.partial = reinterpret_cast<float*>(static_cast<char*>(ws) + region_off + L.partial);
+  p.tickets = reinterpret_cast<int*>(static_cast<char*>(ws) + kWsFfnTicketOffset);
+  p.err = err_word(ws);
+  p.T = T;
+  p.H = H;
+  p.F = F;
+  p.E = E;
+  p.k = k;
+  p.cap_rows = static_cast<int>(cap_rows);
+  p.max_slots = ffn_max_slots(block_m) < kFfnMaxTickets ? ffn_max_slots(block_m) : kFfnMaxTickets;
+  return p;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+const char* moe_status_string(int status) {
+  switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported combination";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_DEVICE: return "device error word set";
+  }
+  return "unknown status";
+}
+
+const char* moe_last_cuda_error_string(void) { return g_last_cuda_error; }
+
+int moe_pick_block_m(int T, int k, int E) {
+  if (E <= 0) return 16;
+  const long long tk = static_cast<long long>(T) * k;
+  if (tk < 8ll * E) return 16;
+  if (tk < 64ll * E) return 64;
+  return 128;
+}
+
+int moe_workspace_init(void* ws, size_t ws_bytes, void* stream) {
+  if (!ws || ws_bytes < kWsHeaderBytes) return MOE_ERR_ARG;
+  const cudaError_t e = cudaMemsetAsync(ws, 0, ws_bytes, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MOE_OK : cuda_fail("cudaMemsetAsync", e);
+}
+
+int moe_read_device_error(void* ws, int32_t* code, int clear, void* stream) {
+  if (!ws || !code) return MOE_ERR_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail("cudaStreamSynchronize", e);
+  int32_t v = 0;
+  e = cudaMemcpy(&v, err_word(ws), sizeof(v), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail("cudaMemcpy", e);
+  *code = v;
+  if (clear && v) {
+    e = cudaMemset(err_word(ws), 0, sizeof(int32_t));
+    if (e != cudaSuccess) return cuda_fail("cudaMemset", e);
+  }
+  return v ? MOE_ERR_DEVICE : MOE_OK;
+}
+
+// ---- router -------------------------------------------------------------------
+size_t moe_router_workspace_bytes(int T, int H, int E) {
+  if (T < 0 || H <= 0 || E <= 0) return 0;
+  return kWsHeaderBytes + plan_router(T, H, E).scratch_bytes;
+}
+
+int moe_router(const void* hidden, int hidden_dt, const uint8_t* hidden_scale, const void* gate,
+               int gate_dt, const float* bias, int T, int H, int E, int k, int scoring,
+               int n_group, int topk_group, int renormalize, float scaling, int32_t* topk_ids,
+               float* topk_weights, void* ws, size_t ws_bytes, void* stream) {
+  int rc = check_router(hidden, hidden_dt, hidden_scale, gate, gate_dt, T, H, E, k, scoring,
+                        n_group, topk_group);
+  if (rc != MOE_OK) return rc;
+  if (T == 0) return MOE_OK;
+  if (!topk_ids || !topk_weights || !ws) return MOE_ERR_ARG;
+  if (ws_bytes < moe_router_workspace_bytes(T, H, E) || !aligned(ws, 256)) return MOE_ERR_ARG;
+  const RouterPlan plan = plan_router(T, H, E);
+  char* base = static_cast<char*>(ws);
+  if (launch_router(hidden, hidden_dt, hidden_scale, gate, gate_dt, bias, T, H, E, k, scoring,
+                    n_group, topk_group, renormalize, scaling, topk_ids, topk_weights,
+                    reinterpret_cast<float*>(base + kWsHeaderBytes),
+                    reinterpret_cast<int*>(base + kWsRouterTicketOffset), err_word(ws), plan,
+                    static_cast<cudaStream_t>(stream)) != 0)
+    return launch_fail("router kernel");
+  return MOE_OK;
+}
+
+// ---- align --------------------------------------------------------------------
+size_t moe_align_workspace_bytes(void) { return kWsHeaderBytes; }
+
+int moe_align(const int32_t* topk_ids, int T, int k, int E, int block_m, int32_t* sorted_ids,
+              int64_t cap_rows, int32_t* block_expert, int32_t* num_post_padded, void* ws,
+              size_t ws_bytes, void* stream) {
+  if (T < 0 || k <= 0 || E <= 0 || E > 1024) return MOE_ERR_ARG;
+  if (check_block_m(block_m) != MOE_OK) return MOE_ERR_ARG;
+  if (cap_rows < static_cast<int64_t>(T) * k + static_cast<int64_t>(E) * (block_m - 1) ||
+      cap_rows > 0x7fffffffll)
+    return MOE_ERR_ARG;
+  if ((T > 0 && !topk_ids) || !sorted_ids || !block_expert || !num_post_padded || !ws)
+    return MOE_ERR_ARG;
+  if (ws_bytes < kWsHeaderBytes) return MOE_ERR_ARG;
+  if (launch_align(topk_ids, T, k, E, block_m, sorted_ids, cap_rows, block_expert,
+                   num_post_padded, err_word(ws), static_cast<cudaStream_t>(stream)) != 0)
+    return launch_fail("align kernel");
+  return MOE_OK;
+}
+
+// ---- expert GEMMs --------------------------------------------------------------
+size_t moe_ffn_workspace_bytes(int T, int H, int F, int E, int k, int block_m, int act_dt) {
+  (void)H;
+  (void)act_dt;
+  if (T < 0 || F <= 0 || E <= 0 || k <= 0 || check_block_m(block_m) != MOE_OK) return 0;
+  return kWsHeaderBytes + ffn_layout(T, F, E, k, block_m, true).total;
+}
+
+static int expert_gemm(int kind, const void* act, int act_dt, const void* w, int w_dt, int T,
+                       int H, int F, int E, int k, int block_m, const int32_t* sorted_ids,
+                       const int32_t* block_expert, const int32_t* npp, int64_t cap_rows,
+                       void* inter, const float* topk_weights, void* stage, void* ws,
+                       size_t ws_bytes, bool inter_in_ws, cudaStream_t stream) {
+  int rc = check_ffn(act_dt, w_dt, T, H, F, E, k, block_m, cap_rows);
+  if (rc != MOE_OK) return rc;
+  if (T == 0) return MOE_OK;
+  if (!act || !w || !sorted_ids || !block_expert || !npp || !ws) return MOE_ERR_ARG;
+  if (kind == 0 && !inter) return MOE_ERR_ARG;
+  if (kind == 1 && (!topk_weights || !stage)) return MOE_ERR_ARG;
+  if (!aligned(ws, 256) || !aligned(act, 16) || !aligned(w, 16) || (inter && !aligned(inter, 16)) ||
+      (stage && !aligned(stage, 16)))
+    return MOE_ERR_ARG;
+  const FfnLayout L = ffn_layout(T, F, E, k, block_m, inter_in_ws);
+  if (ws_bytes < kWsHeaderBytes + L.total) return MOE_ERR_ARG;
+  FfnParams p = ffn_params(T, H, F, E, k, block_m, sorted_ids, block_expert, npp, cap_rows, ws,
+                           kWsHeaderBytes, L);
+  if (kind == 0) {
+    p.x = act;
+    p.inter = inter;
+  } else {
+    p.inter = const_cast<void*>(act);
+    p.topk_weights = topk_weights;
+    p.stage = stage;
+  }
+  const int sms = device_num_sms();
+  if (sms <= 0) return cuda_fail("cudaDeviceGetAttribute", cudaGetLastError());
+  const char* why = "";
+  if (launch_ffn_gemm(kind, block_m, w, p, sms, stream, &why) != 0) return launch_fail(why);
+  return MOE_OK;
+}
+
+int moe_expert_gemm1(const void* x, int act_dt, const uint8_t* x_scale, const void* w13,
+                     const uint8_t* w13_scale, int w_dt, int T, int H, int F, int E, int k,
+                     int block_m, const int32_t* sorted_ids, const int32_t* block_expert,
+                     const int32_t* num_post_padded, int64_t cap_rows, void* inter,
+                     uint8_t* inter_scale, void* ws, size_t ws_bytes, void* stream) {
+  (void)x_scale;
+  (void)w13_scale;
+  (void)inter_scale;
+  return expert_gemm(0, x, act_dt, w13, w_dt, T, H, F, E, k, block_m, sorted_ids, block_expert,
+                     num_post_padded, cap_rows, inter, nullptr, nullptr, ws, ws_bytes, false,
+                     static_cast<cudaStream_t>(stream));
+}
+
+int moe_expert_gemm2(const void* inter, const uint8_t* inter_scale, int act_dt, const void* w2,
+                     const uint8_t* w2_scale, int w_dt, int T, int H, int F, int E, int k,
+                     int block_m, const int32_t* sorted_ids, const int32_t* block_expert,
+                     const int32_t* num_post_padded, int64_t cap_rows,
+                     const float* topk_weights, void* stage, void* ws, size_t ws_bytes,
+                     void* stream) {
+  (void)inter_scale;
+  (void)w2_scale;
+  return expert_gemm(1, inter, act_dt, w2, w_dt, T, H, F, E, k, block_m, sorted_ids,
+                     block_expert, num_post_padded, cap_rows, nullptr, topk_weights, stage, ws,
+                     ws_bytes, false, static_cast<cudaStream_t>(stream));
+}
+
+int moe_grouped_ffn(const void* x, const uint8_t* x_scale, int act_dt, const void* w13,
+                    const uint8_t* w13_scale, const void* w2, const uint8_t* w2_scale, int w_dt,
+                    int T, int H, int F, int E, int k, int block_m, const int32_t* sorted_ids,
+                    const int32_t* block_expert, const int32_t* num_post_padded,
+                    int64_t cap_rows, const float* topk_weights, void* stage, void* ws,
+                    size_t ws_bytes, void* stream) {
+  (void)x_scale;
+  (void)w13_scale;
+  (void)w2_scale;
+  int rc = check_ffn(act_dt, w_dt, T, H, F, E, k, block_m, cap_rows);
+  if (rc != MOE_OK) return rc;
+  if (T == 0) return MOE_OK;
+  if (!ws) return MOE_ERR_ARG;
+  if (ws_bytes < moe_ffn_workspace_bytes(T, H, F, E, k, block_m, act_dt)) return MOE_ERR_ARG;
+  if (cap_rows != static_cast<int64_t>(T) * k + static_cast<int64_t>(E) * (block_m - 1))
+    return MOE_ERR_ARG;  // the workspace holds exactly the worst-case intermediate
+  const FfnLayout L = ffn_layout(T, F, E, k, block_m, true);
+  void* inter = static_cast<char*>(ws) + kWsHeaderBytes + L.inter;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  rc = expert_gemm(0, x, act_dt, w13, w_dt, T, H, F, E, k, block_m, sorted_ids, block_expert,
+                   num_post_padded, cap_rows, inter, nullptr, nullptr, ws, ws_bytes, true, s);
+  if (rc != MOE_OK) return rc;
+  return expert_gemm(1, inter, act_dt, w2, w_dt, T, H, F, E, k, block_m, sorted_ids,
+                     block_expert, num_post_padded, cap_rows, nullptr, topk_weights, stage, ws,
+                     ws_bytes, true, s);
+}
+
+// ---- finalize -------------------------------------------------------------------
+int moe_finalize(const void* stage, int T, int k, int H, void* out, void* stream) {
+  if (T < 0 || k <= 0 || H <= 0 || H % 8 != 0) return MOE_ERR_ARG;
+  if (T == 0) return MOE_OK;
+  if (!stage || !out || !aligned(stage, 16) || !aligned(out, 16)) return MOE_ERR_ARG;
+  if (launch_finalize(stage, T, k, H, out, static_cast<cudaStream_t>(stream)) != 0)
+    return launch_fail("finalize kernel");
+  return MOE_OK;
+}
+
+// ---- layer ------------------------------------------------------------------------
+size_t moe_layer_workspace_bytes(int T, int H, int F, int E, int k, int block_m, int act_dt) {
+  (void)act_dt;
+  if (T < 0 || H <= 0 || F <= 0 || E <= 0 || k <= 0) return 0;
+  if (block_m == 0) block_m = moe_pick_block_m(T, k, E);
+  if (check_block_m(block_m) != MOE_OK) return 0;
+  return layer_layout(T, H, F, E, k, block_m).total;
+}
+
+int moe_layer(const void* hidden, int act_dt, const uint8_t* hidden_scale, const void* gate,
+              int gate_dt, const float* bias, const void* w13, const uint8_t* w13_scale,
+              const void* w2, const uint8_t* w2_scale, int w_dt, int T, int H, int F, int E,
+              int k, int scoring, int n_group, int topk_group, int renormalize, float scaling,
+              int block_m, void* out, void* ws, size_t ws_bytes, void* stream) {
+  if (block_m == 0) block_m = moe_pick_block_m(T, k, E);
+  int rc = check_router(hidden, act_dt, hidden_scale, gate, gate_dt, T, H, E, k, scoring,
+                        n_group, topk_group);
+  if (rc != MOE_OK) return rc;
+  const LayerLayout L = layer_layout(T, H, F, E, k, block_m);
+  rc = check_ffn(act_dt, w_dt, T, H, F, E, k, block_m, L.cap);
+  if (rc != MOE_OK) return rc;
+  if (T == 0) return MOE_OK;
+  if (!out || !ws || !w13 || !w2) return MOE_ERR_ARG;
+  if (ws_bytes < L.total || !aligned(ws, 256)) return MOE_ERR_ARG;
+  char* base = static_cast<char*>(ws);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t* ids = reinterpret_cast<int32_t*>(base + L.ids);
+  float* wts = reinterpret_cast<float*>(base + L.wts);
+  int32_t* sorted = reinterpret_cast<int32_t*>(base + L.sorted);
+  int32_t* blk = reinterpret_cast<int32_t*>(base + L.blk);
+  int32_t* npp = reinterpret_cast<int32_t*>(base + L.npp);
+  void* stage = base + L.stage;
+  const RouterPlan plan = plan_router(T, H, E);
+  if (launch_router(hidden, act_dt, hidden_scale, gate, gate_dt, bias, T, H, E, k, scoring,
+                    n_group, topk_group, renormalize, scaling, ids, wts,
+                    reinterpret_cast<float*>(base + L.router),
+                    reinterpret_cast<int*>(base + kWsRouterTicketOffset), err_word(ws), plan,
+                    s) != 0)
+    return launch_fail("router kernel");
+  if (launch_align(ids, T, k, E, block_m, sorted, L.cap, blk, npp, err_word(ws), s) != 0)
+    return launch_fail("align kernel");
+  const FfnLayout FL = ffn_layout(T, F, E, k, block_m, true);
+  void* inter = base + L.ffn + FL.inter;
+  FfnParams p = ffn_params(T, H, F, E, k, block_m, sorted, blk, npp, L.cap, ws, L.ffn, FL);
+  const int sms = device_num_sms();
+  if (sms <= 0) return cuda_fail("cudaDeviceGetAttribute", cudaGetLastError());
+  const char* why = "";
+  p.x = hidden;
+  p.inter = inter;
+  if (launch_ffn_gemm(0, block_m, w13, p, sms, s, &why) != 0) return launch_fail(why);
+  p.topk_weights = wts;
+  p.stage = stage;
+  if (launch_ffn_gemm(1, block_m, w2, p, sms, s, &why) != 0) return launch_fail(why);
+  if (launch_finalize(stage, T, k, H, out, s) != 0) return launch_fail("finalize kernel");
+  return MOE_OK;
+}
+
+}  // extern "C"

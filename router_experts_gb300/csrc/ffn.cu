@@ -1,0 +1,576 @@
+// ffn.cu -- the grouped expert GEMMs on the 5th-generation tensor cores.
+//
+// Follows "MoE Kernels, in depth", The fused expert GEMM (every tile looks up
+// its expert in block_expert and its rows in sorted_ids, the activation gather
+// is folded into the operand load, padding rows are masked, gate and up form
+// one 2F x H matrix with SwiGLU in the epilogue, the routing weight is applied
+// in the down GEMM's epilogue) and "Mixture of Experts" (w13 [E, 2F, H] with
+// the gate rows first, w2 [E, H, F]; row = sorted id // top_k).
+//
+// One persistent kernel per GEMM, one CTA per SM, 8 warps:
+//   warp 0      TMA producer: expert weight tiles (and, for GEMM2, the
+//               intermediate rows) into a ring of shared-memory stages
+//   warp 1      TMEM allocator and the single thread issuing tcgen05.mma
+//   warps 2-3   GEMM1 only: gather of the token rows x[sorted_id / k] with
+//               16-byte cp.async straight into the 128-byte-swizzled operand
+//               layout (zero-filled for padding rows)
+//   warps 4-7   epilogue: TMEM -> registers -> SwiGLU / routing weight ->
+//               global memory; two TMEM accumulators so the epilogue of one
+//               tile overlaps the MMAs of the next
+//
+// Tile orientation depends on the tile height BM (rows per expert block):
+//   BM = 128: A = 128 token rows (M = 128), B = 256 weight rows (N = 256);
+//             GEMM1 loads the 128 gate rows and the matching 128 up rows as
+//             two boxes so the epilogue pairs column c with column c + 128.
+//   BM = 16/64 ("swap"): A = 128 weight rows (M = 128), B = the BM token rows
+//             (N = BM); GEMM1 issues two MMAs per K step (gate rows, up rows)
+//             into two accumulators.  Few tokens per expert is the decode
+//             regime, which streams weights: when the tiles are too few to
+//             fill the GPU the K range is split (chosen on the device from the
+//             padded length) and the last split to finish (atomic ticket, no
+//             spinning) sums the fp32 partials in split order and runs the
+//             epilogue.
+#include "moe_common.cuh"
+#include "moe_internal.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kBK = 64;                 // K elements per stage (128 bytes of bf16)
+constexpr int kStageBudget = 220 * 1024;
+
+template <int KIND, int BM>
+struct Cfg {
+  static constexpr bool SWAP = BM < 128;
+  static constexpr bool GATHER = KIND == 0;
+  static constexpr int NT = (KIND == 0) ? 128 : (SWAP ? 128 : 256);  // output tile width
+  static constexpr int A_BYTES = (KIND == 0 && SWAP) ? 2 * 128 * 128 : 128 * 128;
+  static constexpr int B_ROWS = SWAP ? BM : 256;
+  static constexpr int B_BYTES = B_ROWS * 128;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES_RAW = kStageBudget / STAGE_BYTES;
+  static constexpr int STAGES = STAGES_RAW > 12 ? 12 : STAGES_RAW;
+  static constexpr int ACC_COLS = (KIND == 0 && SWAP) ? 2 * BM : (SWAP ? BM : 256);
+  static constexpr int TMEM_COLS = (2 * ACC_COLS <= 32)    ? 32
+                                   : (2 * ACC_COLS <= 64)  ? 64
+                                   : (2 * ACC_COLS <= 128) ? 128
+                                   : (2 * ACC_COLS <= 256) ? 256
+                                                           : 512;
+  // bytes delivered by TMA per stage
+  static constexpr int TX_BYTES = GATHER ? (SWAP ? A_BYTES : B_BYTES) : STAGE_BYTES;
+  static constexpr uint32_t IDESC = SWAP ? idesc_bf16_f32(128, BM) : idesc_bf16_f32(128, 256);
+  // gather: rows of the token tile, 16-byte chunks per thread per stage
+  static constexpr int G_ROWS = SWAP ? BM : 128;
+  static constexpr int G_PER_THREAD = G_ROWS / 8;  // 64 threads, 8 chunks per row
+  static constexpr int G_LAG = (STAGES - 1) < 3 ? (STAGES - 1) : 3;
+  static constexpr int BAR_BYTES = 256;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + BAR_BYTES;
+  static_assert(STAGE_BYTES % 1024 == 0, "stage tiles must keep 1024-byte alignment");
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+};
+
+// Split count for the swap tiles: minimise (waves x k-blocks per unit) with a
+// per-unit overhead of one k-block, within the partial-sum capacity.
+MOE_DEV int choose_splits(int ug, int KB, int ctas, int max_slots) {
+  if (ug <= 0) return 1;
+  int best_s = 1;
+  long long best = 0x7fffffffffffffffll;
+  for (int s = 1; s <= 32 && s <= KB; ++s) {
+    if (s > 1 && static_cast<long long>(ug) * s > max_slots) break;
+    const long long waves = (static_cast<long long>(ug) * s + ctas - 1) / ctas;
+    const long long cost = waves * ((KB + s - 1) / s + 1);
+    if (cost < best) {
+      best = cost;
+      best_s = s;
+    }
+  }
+  return best_s;
+}
+
+struct Sched {
+  int nblk, ntiles, KB, S, num_units;
+};
+
+template <int KIND, int BM>
+MOE_DEV Sched make_sched(const FfnParams& p) {
+  using C = Cfg<KIND, BM>;
+  Sched s;
+  int npp = __ldg(p.num_post_padded);
+  npp = max(0, min(npp, p.cap_rows));
+  s.nblk = npp / BM;
+  s.ntiles = (KIND == 0) ? (p.F + C::NT - 1) / C::NT : (p.H + C::NT - 1) / C::NT;
+  const int K = (KIND == 0) ? p.H : p.F;
+  s.KB = (K + kBK - 1) / kBK;
+  s.S = C::SWAP ? choose_splits(s.nblk * s.ntiles, s.KB, gridDim.x, p.max_slots) : 1;
+  s.num_units = s.nblk * s.ntiles * s.S;
+  return s;
+}
+
+struct Unit {
+  int b, n, s, ug, kb0, kb1, e;
+};
+
+template <int KIND, int BM>
+MOE_DEV Unit decode_unit(const FfnParams& p, const Sched& sc, int u) {
+  Unit x;
+  x.s = u % sc.S;
+  x.ug = u / sc.S;
+  x.b = x.ug / sc.ntiles;
+  x.n = x.ug % sc.ntiles;
+  x.kb0 = static_cast<int>(static_cast<long long>(x.s) * sc.KB / sc.S);
+  x.kb1 = static_cast<int>(static_cast<long long>(x.s + 1) * sc.KB / sc.S);
+  int e = __ldg(p.block_expert + x.b);
+  if (e < 0 || e >= p.E) {
+    if (threadIdx.x == 0) raise_error(p.err, kErrBadTable);
+    e = min(max(e, 0), p.E - 1);
+  }
+  x.e = e;
+  return x;
+}
+
+// 16 fp32 accumulator columns of this thread's TMEM lane.
+MOE_DEV void load_cols(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  tmem_ld16(taddr, r);
+  tmem_ld_wait();
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// 16 summed split-K partial columns of one row (split order 0..S-1).
+MOE_DEV void load_partial_cols(const float* base, size_t slot_stride, int S, float (&v)[16]) {
+#pragma unroll
+  for (int i = 0; i < 16; i += 4) {
+    float4 t = __ldcg(reinterpret_cast<const float4*>(base + i));
+    v[i] = t.x;
+    v[i + 1] = t.y;
+    v[i + 2] = t.z;
+    v[i + 3] = t.w;
+  }
+  for (int s = 1; s < S; ++s) {
+    const float* b = base + s * slot_stride;
+#pragma unroll
+    for (int i = 0; i < 16; i += 4) {
+      float4 t = __ldcg(reinterpret_cast<const float4*>(b + i));
+      v[i] += t.x;
+      v[i + 1] += t.y;
+      v[i + 2] += t.z;
+      v[i + 3] += t.w;
+    }
+  }
+}
+
+// Epilogue of one output tile for the thread owning accumulator row `row`.
+// `fetch(col, v)` returns 16 accumulator columns starting at `col`.
+template <int KIND, int BM, class Fetch>
+MOE_DEV void epilogue_tile(const FfnParams& p, const Unit& u, int row, Fetch&& fetch) {
+  using C = Cfg<KIND, BM>;
+  const int nk = p.T * p.k;
+  if constexpr (KIND == 0 && C::SWAP) {
+    // row = feature f0 + row; columns: gate tokens [0, BM), up tokens [BM, 2BM)
+    const int f = u.n * C::NT + row;
+    __nv_bfloat16* inter = reinterpret_cast<__nv_bfloat16*>(p.inter);
+#pragma unroll 1
+    for (int c0 = 0; c0 < BM; c0 += 16) {
+      float g[16], v[16];
+      fetch(c0, g);
+      fetch(BM + c0, v);
+      if (f < p.F) {
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const size_t prow = static_cast<size_t>(u.b) * BM + c0 + c;
+          inter[prow * p.F + f] = __float2bfloat16_rn(silu_f(g[c]) * v[c]);
+        }
+      }
+    }
+  } else if constexpr (KIND == 0) {
+    // row = token row of the block; columns: gate features [0,128), up [128,256)
+    const size_t prow = static_cast<size_t>(u.b) * BM + row;
+    __nv_bfloat16* inter = reinterpret_cast<__nv_bfloat16*>(p.inter);
+#pragma unroll 1
+    for (int c0 = 0; c0 < 128; c0 += 16) {
+      float g[16], v[16];
+      fetch(c0, g);
+      fetch(128 + c0, v);
+      const int f = u.n * C::NT + c0;
+      if (f + 16 <= p.F) {
+        uint32_t w[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          w[i] = pack_bf16x2(silu_f(g[2 * i]) * v[2 * i], silu_f(g[2 * i + 1]) * v[2 * i + 1]);
+        uint4* dst = reinterpret_cast<uint4*>(inter + prow * p.F + f);
+        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+      }
+    }
+  } else if constexpr (C::SWAP) {
+    // row = output column h of the layer; columns: the block's tokens
+    const int h = u.n * C::NT + row;
+    __nv_bfloat16* stage = reinterpret_cast<__nv_bfloat16*>(p.stage);
+#pragma unroll 1
+    for (int c0 = 0; c0 < BM; c0 += 16) {
+      float v[16];
+      fetch(c0, v);
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const int a = __ldg(p.sorted_ids + static_cast<size_t>(u.b) * BM + c0 + c);
+        if (a >= 0 && a < nk && h < p.H) {
+          const float w = __ldg(p.topk_weights + a);
+          stage[static_cast<size_t>(a) * p.H + h] = __float2bfloat16_rn(v[c] * w);
+        }
+      }
+    }
+  } else {
+    // row = token row of the block; columns: output columns h
+    const int a = __ldg(p.sorted_ids + static_cast<size_t>(u.b) * BM + row);
+    const bool valid = a >= 0 && a < nk;
+    const float w = valid ? __ldg(p.topk_weights + a) : 0.f;
+    __nv_bfloat16* stage = reinterpret_cast<__nv_bfloat16*>(p.stage);
+#pragma unroll 1
+    for (int c0 = 0; c0 < 256; c0 += 16) {
+      float v[16];
+      fetch(c0, v);
+      const int h = u.n * C::NT + c0;
+      if (valid && h + 16 <= p.H) {
+        uint32_t o[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) o[i] = pack_bf16x2(v[2 * i] * w, v[2 * i + 1] * w);
+        uint4* dst = reinterpret_cast<uint4*>(stage + static_cast<size_t>(a) * p.H + h);
+        dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+        dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+      }
+    }
+  }
+}
+
+template <int KIND, int BM>
+__global__ void __launch_bounds__(kThreads, 1)
+    ffn_gemm_kernel(const __grid_constant__ CUtensorMap tm_w,
+                    const __grid_constant__ CUtensorMap tm_in, const FfnParams p) {
+  using C = Cfg<KIND, BM>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
+  uint64_t* empty_bar = full_bar + C::STAGES;
+  uint64_t* tfull_bar = empty_bar + C::STAGES;
+  uint64_t* tempty_bar = tfull_bar + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty_bar + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* last_flag = abort_flag + 1;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const Sched sc = make_sched<KIND, BM>(p);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::STAGES; ++i) {
+      mbar_init(&full_bar[i], 1 + (C::GATHER ? 64 : 0));
+      mbar_init(&empty_bar[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&tfull_bar[i], 1);
+      mbar_init(&tempty_bar[i], 4);
+    }
+    *abort_flag = 0;
+    *last_flag = 0;
+    mbar_fence_init();
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, C::TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_w);
+      if (KIND == 1) tma_prefetch_desc(&tm_in);
+      uint32_t it = 0;
+      bool alive = true;
+      for (int uu = blockIdx.x; alive && uu < sc.num_units; uu += gridDim.x) {
+        const Unit u = decode_unit<KIND, BM>(p, sc, uu);
+        for (int kb = u.kb0; kb < u.kb1; ++kb, ++it) {
+          const int st = it % C::STAGES;
+          const uint32_t ph = (it / C::STAGES) & 1u;
+          if (!mbar_wait(&empty_bar[st], ph ^ 1u, abort_flag, p.err)) {
+            alive = false;
+            break;
+          }
+          uint8_t* sa = smem + st * C::STAGE_BYTES;
+          uint8_t* sb = sa + C::A_BYTES;
+          mbar_arrive_expect_tx(&full_bar[st], C::TX_BYTES);
+          const int kc = kb * kBK;
+          if constexpr (KIND == 0) {
+            const int grow = u.e * 2 * p.F + u.n * C::NT;
+            const int urow = grow + p.F;
+            uint8_t* dst = C::SWAP ? sa : sb;
+            tma_load_2d(dst, &tm_w, &full_bar[st], kc, grow);
+            tma_load_2d(dst + 128 * 128, &tm_w, &full_bar[st], kc, urow);
+          } else {
+            const int wrow = u.e * p.H + u.n * C::NT;
+            if constexpr (C::SWAP) {
+              tma_load_2d(sa, &tm_w, &full_bar[st], kc, wrow);
+              tma_load_2d(sb, &tm_in, &full_bar[st], kc, u.b * BM);
+            } else {
+              tma_load_2d(sa, &tm_in, &full_bar[st], kc, u.b * BM);
+              tma_load_2d(sb, &tm_w, &full_bar[st], kc, wrow);
+            }
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      uint32_t it = 0, acc_it = 0;
+      bool alive = true;
+      for (int uu = blockIdx.x; alive && uu < sc.num_units; uu += gridDim.x, ++acc_it) {
+        const Unit u = decode_unit<KIND, BM>(p, sc, uu);
+        const int buf = acc_it & 1;
+        const uint32_t aph = (acc_it >> 1) & 1u;
+        if (!mbar_wait(&tempty_bar[buf], aph ^ 1u, abort_flag, p.err)) break;
+        tc_fence_after();
+        const uint32_t d = tmem_base + buf * C::ACC_COLS;
+        for (int kb = u.kb0; kb < u.kb1; ++kb, ++it) {
+          const int st = it % C::STAGES;
+          const uint32_t ph = (it / C::STAGES) & 1u;
+          if (!mbar_wait(&full_bar[st], ph, abort_flag, p.err)) {
+            alive = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(smem + st * C::STAGE_BYTES);
+          const uint32_t b_addr = a_addr + C::A_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            const uint32_t acc = (kb > u.kb0 || kk > 0) ? 1u : 0u;
+            const uint64_t bdesc = sw128_desc(b_addr + kk * 32);
+            if constexpr (KIND == 0 && C::SWAP) {
+              umma_f16(d, sw128_desc(a_addr + kk * 32), bdesc, C::IDESC, acc);
+              umma_f16(d + BM, sw128_desc(a_addr + 128 * 128 + kk * 32), bdesc, C::IDESC, acc);
+            } else {
+              umma_f16(d, sw128_desc(a_addr + kk * 32), bdesc, C::IDESC, acc);
+            }
+          }
+          umma_commit(&empty_bar[st]);
+        }
+        if (!alive) break;
+        umma_commit(&tfull_bar[buf]);
+      }
+    }
+  } else if (warp < 4) {
+    // ---------------- token-row gather (GEMM1) ----------------
+    if constexpr (C::GATHER) {
+      const int gt = threadIdx.x - 64;  // 0..63
+      const int chunk = gt & 7;
+      const __nv_bfloat16* x = reinterpret_cast<const __nv_bfloat16*>(p.x);
+      const int nk = p.T * p.k;
+      uint32_t it = 0;
+      int pending = 0;
+      bool alive = true;
+      for (int uu = blockIdx.x; alive && uu < sc.num_units; uu += gridDim.x) {
+        const Unit u = decode_unit<KIND, BM>(p, sc, uu);
+        const __nv_bfloat16* src[C::G_PER_THREAD];
+        uint32_t nbytes[C::G_PER_THREAD];
+#pragma unroll
+        for (int i = 0; i < C::G_PER_THREAD; ++i) {
+          const int r = (gt >> 3) + 8 * i;
+          const int a = __ldg(p.sorted_ids + static_cast<size_t>(u.b) * BM + r);
+          const bool valid = a >= 0 && a < nk;
+          src[i] = valid ? x + static_cast<size_t>(a / p.k) * p.H + chunk * 8 : x;
+          nbytes[i] = valid ? 16u : 0u;
+        }
+        for (int kb = u.kb0; kb < u.kb1; ++kb, ++it) {
+          const int st = it % C::STAGES;
+          const uint32_t ph = (it / C::STAGES) & 1u;
+          if (!mbar_wait(&empty_bar[st], ph ^ 1u, abort_flag, p.err)) {
+            alive = false;
+            break;
+          }
+          const uint32_t tile = smem_u32(smem + st * C::STAGE_BYTES) + (C::SWAP ? C::A_BYTES : 0);
+#pragma unroll
+          for (int i = 0; i < C::G_PER_THREAD; ++i) {
+            const int r = (gt >> 3) + 8 * i;
+            const uint32_t dst = tile + r * 128 + ((chunk ^ (r & 7)) << 4);
+            cp_async_16(dst, nbytes[i] ? src[i] + kb * kBK : src[i], nbytes[i]);
+          }
+          cp_async_commit();
+          ++pending;
+          if (pending > C::G_LAG) {
+            cp_async_wait<C::G_LAG>();
+            fence_proxy_async_smem();
+            mbar_arrive(&full_bar[(it - C::G_LAG) % C::STAGES]);
+            --pending;
+          }
+        }
+      }
+      cp_async_wait<0>();
+      fence_proxy_async_smem();
+      if (alive) {
+        for (int j = pending; j > 0; --j) mbar_arrive(&full_bar[(it - j) % C::STAGES]);
+      }
+    }
+  } else {
+    // ---------------- epilogue ----------------
+    const int ew = warp - 4;
+    const int row = ew * 32 + lane;
+    const int et = threadIdx.x - 128;
+    uint32_t acc_it = 0;
+    for (int uu = blockIdx.x; uu < sc.num_units; uu += gridDim.x, ++acc_it) {
+      const Unit u = decode_unit<KIND, BM>(p, sc, uu);
+      const int buf = acc_it & 1;
+      const uint32_t aph = (acc_it >> 1) & 1u;
+      // every epilogue thread takes the same decision to stop
+      const bool ok = mbar_wait(&tfull_bar[buf], aph, abort_flag, p.err);
+      if (named_bar_any(1, 128, !ok || *abort_flag)) break;
+      tc_fence_after();
+      const uint32_t tb = tmem_base + (static_cast<uint32_t>(ew * 32) << 16) + buf * C::ACC_COLS;
+      if (sc.S == 1) {
+        epilogue_tile<KIND, BM>(p, u, row,
+                                [&](int col, float (&v)[16]) { load_cols(tb + col, v); });
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty_bar[buf]);
+      } else {
+        // split-K: publish this split's partial, the last split finishes
+        const size_t slot_stride = static_cast<size_t>(128) * C::ACC_COLS;
+        float* mine = p.partial + (static_cast<size_t>(u.ug) * sc.S + u.s) * slot_stride +
+                      static_cast<size_t>(row) * C::ACC_COLS;
+#pragma unroll 1
+        for (int c0 = 0; c0 < C::ACC_COLS; c0 += 16) {
+          float v[16];
+          load_cols(tb + c0, v);
+#pragma unroll
+          for (int i = 0; i < 16; i += 4)
+            __stcg(reinterpret_cast<float4*>(mine + c0 + i), make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]));
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty_bar[buf]);
+        __threadfence();
+        named_bar_sync(1, 128);
+        if (et == 0) {
+          const int old = atomicAdd(p.tickets + u.ug, 1);
+          const int last = (old == sc.S - 1);
+          if (last) p.tickets[u.ug] = 0;  // ready for the next launch
+          *last_flag = last;
+        }
+        named_bar_sync(1, 128);
+        if (*last_flag) {
+          __threadfence();
+          const float* base0 = p.partial + static_cast<size_t>(u.ug) * sc.S * slot_stride +
+                               static_cast<size_t>(row) * C::ACC_COLS;
+          epilogue_tile<KIND, BM>(p, u, row, [&](int col, float (&v)[16]) {
+            load_partial_cols(base0 + col, slot_stride, sc.S, v);
+          });
+        }
+      }
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encoder() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  }
+  return fn;
+}
+
+// 2-D bf16 map of a row-major [rows, cols] matrix; box = 64 columns x box_rows.
+bool make_map_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
+                   uint32_t box_rows) {
+  EncodeTiledFn enc = get_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int KIND, int BM>
+int launch_kind(const CUtensorMap& tw, const CUtensorMap& tin, const FfnParams& p, int num_sms,
+                cudaStream_t stream) {
+  using C = Cfg<KIND, BM>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(ffn_gemm_kernel<KIND, BM>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::SMEM_BYTES) != cudaSuccess)
+      return -1;
+    attr_set = true;
+  }
+  ffn_gemm_kernel<KIND, BM><<<num_sms, kThreads, C::SMEM_BYTES, stream>>>(tw, tin, p);
+  return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
+
+}  // namespace
+
+int ffn_max_slots(int block_m) { return block_m == 16 ? 1024 : (block_m == 64 ? 256 : 0); }
+
+size_t ffn_partial_bytes(int block_m) {
+  // GEMM1 (two accumulators of block_m columns) needs the most per slot
+  return align_up(static_cast<size_t>(ffn_max_slots(block_m)) * 128 * 2 * block_m * 4, 256);
+}
+
+int launch_ffn_gemm(int kind, int block_m, const void* w, const FfnParams& p, int num_sms,
+                    cudaStream_t stream, const char** why) {
+  CUtensorMap tw, tin;
+  const bool swap = block_m < 128;
+  if (kind == 0) {
+    // w13 [E*2F, H], box 64 x 128
+    if (!make_map_bf16(&tw, w, static_cast<uint64_t>(p.E) * 2 * p.F, p.H, 128)) {
+      *why = "cuTensorMapEncodeTiled failed for w13";
+      return -1;
+    }
+    tin = tw;
+  } else {
+    if (!make_map_bf16(&tw, w, static_cast<uint64_t>(p.E) * p.H, p.F, swap ? 128 : 256)) {
+      *why = "cuTensorMapEncodeTiled failed for w2";
+      return -1;
+    }
+    if (!make_map_bf16(&tin, p.inter, static_cast<uint64_t>(p.cap_rows), p.F, block_m)) {
+      *why = "cuTensorMapEncodeTiled failed for the intermediate";
+      return -1;
+    }
+  }
+  int rc = -1;
+  if (kind == 0) {
+    if (block_m == 16) rc = launch_kind<0, 16>(tw, tin, p, num_sms, stream);
+    else if (block_m == 64) rc = launch_kind<0, 64>(tw, tin, p, num_sms, stream);
+    else rc = launch_kind<0, 128>(tw, tin, p, num_sms, stream);
+  } else {
+    if (block_m == 16) rc = launch_kind<1, 16>(tw, tin, p, num_sms, stream);
+    else if (block_m == 64) rc = launch_kind<1, 64>(tw, tin, p, num_sms, stream);
+    else rc = launch_kind<1, 128>(tw, tin, p, num_sms, stream);
+  }
+  if (rc != 0) *why = "kernel launch failed";
+  return rc;
+}
+
+}  // namespace moe

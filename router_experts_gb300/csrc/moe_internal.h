@@ -1,0 +1,71 @@
+// moe_internal.h -- host-side declarations shared by the translation units of
+// the CUDA library (kernel launchers, workspace layout).  Not part of the ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace moe {
+
+// ---- fixed workspace header (offsets independent of shapes, so a workspace
+// zeroed once stays valid across calls of any shape) --------------------------
+constexpr size_t kWsErrOffset = 0;                  // int32 sticky error word
+constexpr size_t kWsFfnTicketOffset = 1024;         // int32[kFfnMaxTickets]
+constexpr int kFfnMaxTickets = 1024;
+constexpr size_t kWsRouterTicketOffset = 8192;      // int32[kRouterMaxTiles]
+constexpr int kRouterMaxTiles = 65536;              // token tiles of 16 -> T <= 1,048,576
+constexpr size_t kWsHeaderBytes = kWsRouterTicketOffset + 4ull * kRouterMaxTiles;
+
+constexpr size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// ---- router -----------------------------------------------------------------
+struct RouterPlan {
+  int nb8;        // n8 tiles of experts per CTA (1 or 8)
+  int et;         // experts per CTA
+  int ne;         // expert tiles
+  int nt;         // token tiles of 16
+  int ks;         // K splits across CTAs
+  size_t scratch_bytes;
+};
+RouterPlan plan_router(int T, int H, int E);
+int launch_router(const void* hidden, int hidden_dt, const uint8_t* hidden_scale,
+                  const void* gate, int gate_dt, const float* bias, int T, int H, int E, int k,
+                  int scoring, int n_group, int topk_group, int renormalize, float scaling,
+                  int32_t* topk_ids, float* topk_weights, float* scratch, int* tickets, int* err,
+                  const RouterPlan& plan, cudaStream_t stream);
+
+// ---- align ------------------------------------------------------------------
+int launch_align(const int32_t* topk_ids, int T, int k, int E, int block_m, int32_t* sorted_ids,
+                 int64_t cap_rows, int32_t* block_expert, int32_t* num_post_padded, int* err,
+                 cudaStream_t stream);
+
+// ---- expert GEMMs -------------------------------------------------------------
+struct FfnParams {
+  const int32_t* sorted_ids;
+  const int32_t* block_expert;
+  const int32_t* num_post_padded;
+  const void* x;               // GEMM1 activations [T, H]
+  void* inter;                 // GEMM1 output / GEMM2 input [cap, F]
+  const float* topk_weights;   // GEMM2 row weights [T*k]
+  void* stage;                 // GEMM2 output [T*k, H]
+  float* partial;              // split-K partial sums
+  int* tickets;                // split-K tickets (self-resetting)
+  int* err;
+  int T, H, F, E, k;
+  int cap_rows;
+  int max_slots;               // capacity of `partial`, in units
+};
+int ffn_max_slots(int block_m);
+size_t ffn_partial_bytes(int block_m);
+// kind 0: GEMM1 + SwiGLU, kind 1: GEMM2 + routing weight.
+int launch_ffn_gemm(int kind, int block_m, const void* w, const FfnParams& p, int num_sms,
+                    cudaStream_t stream, const char** why);
+
+// ---- finalize -----------------------------------------------------------------
+int launch_finalize(const void* stage, int T, int k, int H, void* out, cudaStream_t stream);
+
+int device_num_sms();
+
+}  // namespace moe

@@ -1,0 +1,105 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports
+every entry point include/moe.h declares, and rejects invalid arguments on the
+host before launching anything."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from router_experts_gb300 import build, moe
+    build.build()
+    return moe.load()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "moe.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(moe_\w+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for want in ["moe_router", "moe_align", "moe_expert_gemm1", "moe_expert_gemm2",
+                 "moe_grouped_ffn", "moe_finalize", "moe_layer", "moe_read_device_error"]:
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    assert lib.moe_status_string(0) == b"ok"
+    assert lib.moe_status_string(1) == b"invalid argument"
+    assert lib.moe_status_string(2) == b"unsupported combination"
+
+
+def test_pick_block_m_rule(lib):
+    # mean rows per expert T*k/E: < 8 -> 16, < 64 -> 64, else 128
+    assert lib.moe_pick_block_m(1, 8, 128) == 16
+    assert lib.moe_pick_block_m(64, 8, 128) == 16
+    assert lib.moe_pick_block_m(128, 8, 128) == 64
+    assert lib.moe_pick_block_m(512, 8, 128) == 64
+    assert lib.moe_pick_block_m(1024, 8, 128) == 128
+    assert lib.moe_pick_block_m(256, 8, 256) == 64
+    assert lib.moe_pick_block_m(4096, 8, 256) == 128
+
+
+def test_workspace_sizes_grow_with_shape(lib):
+    a = lib.moe_layer_workspace_bytes(1, 2048, 768, 128, 8, 0, 0)
+    b = lib.moe_layer_workspace_bytes(4096, 2048, 768, 128, 8, 0, 0)
+    assert 0 < a < b
+    assert lib.moe_layer_workspace_bytes(16, 64, 32, 8, 2, 33, 0) == 0  # bad block_m
+    assert lib.moe_router_workspace_bytes(1, 4096, 288) > 0
+    assert lib.moe_align_workspace_bytes() > 0
+
+
+def call_router(lib, T=4, H=64, E=8, k=2, scoring=0, n_group=1, topk_group=1, hidden_dt=0,
+                gate_dt=0, hidden=1 << 12, gate=1 << 12, ws=1 << 12, ws_bytes=1 << 30):
+    P = ctypes.c_void_p
+    return lib.moe_router(P(hidden), hidden_dt, None, P(gate), gate_dt, None, T, H, E, k, scoring,
+                          n_group, topk_group, 1, ctypes.c_float(1.0), P(1 << 12), P(1 << 12),
+                          P(ws), ws_bytes, None)
+
+
+def test_router_rejects_bad_arguments_without_launching(lib):
+    # these all fail host validation, so no device pointer is touched
+    assert call_router(lib, k=9) == 1             # k > E
+    assert call_router(lib, H=48) == 1            # H % 32
+    assert call_router(lib, E=513, k=2) == 1      # E > 512
+    assert call_router(lib, n_group=3) == 1       # E % n_group
+    assert call_router(lib, E=8, k=4, n_group=4, topk_group=1) == 1  # too few experts kept
+    assert call_router(lib, scoring=5) == 1
+    assert call_router(lib, hidden_dt=3) == 2     # e2m1 hidden: unsupported
+    assert call_router(lib, gate_dt=2) == 2
+    assert call_router(lib, hidden=(1 << 12) + 2) == 1  # misaligned
+    assert call_router(lib, T=0) == 0             # T = 0 is a no-op
+
+
+def test_align_and_ffn_reject_bad_arguments(lib):
+    P = ctypes.c_void_p
+    # capacity below T*k + E*(BM-1)
+    rc = lib.moe_align(P(4096), 4, 2, 8, 16, P(4096), 8 + 8 * 15 - 1, P(4096), P(4096), P(4096),
+                       1 << 20, None)
+    assert rc == 1
+    rc = lib.moe_align(P(4096), 4, 2, 8, 32, P(4096), 1000, P(4096), P(4096), P(4096), 1 << 20,
+                       None)
+    assert rc == 1  # block_m not in {16, 64, 128}
+    # H not a multiple of 64
+    rc = lib.moe_expert_gemm1(P(4096), 0, None, P(4096), None, 0, 4, 96, 32, 8, 2, 16, P(4096),
+                              P(4096), P(4096), 200, P(4096), None, P(4096), 1 << 30, None)
+    assert rc == 1
+    # mixed bf16 activations with fp4 weights: unsupported
+    rc = lib.moe_expert_gemm1(P(4096), 0, None, P(4096), None, 3, 4, 64, 32, 8, 2, 16, P(4096),
+                              P(4096), P(4096), 200, P(4096), None, P(4096), 1 << 30, None)
+    assert rc == 2
+    assert lib.moe_finalize(P(4096), 4, 2, 60, P(4096), None) == 1  # H % 8
+    assert lib.moe_finalize(P(4096), 0, 2, 64, P(4096), None) == 0  # T = 0

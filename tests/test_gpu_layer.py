@@ -1,0 +1,60 @@
+"""The fused layer (router -> align -> GEMM1+SwiGLU -> GEMM2 -> finalize in one
+call) against the oracle layer (which routes on its own, in fp64) on the same
+seeded inputs, over sampled tokens whose routing margin exceeds 1e-4."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from router_experts_gb300 import moe
+from router_experts_gb300 import workloads as W
+
+from _gpu import GAP_MIN, LAYER_RTOL_BF16, compact_experts, host, oracle_router, rel_err, \
+    sample_tokens
+
+pytestmark = pytest.mark.gpu
+
+
+def layer_case(name, T, ntok, block_m=0, seed=0):
+    w = W.WORKLOADS[name]
+    d = W.make_inputs(w, T, seed=seed, device="cuda")
+    y = moe.layer(d["hidden"], d["gate"], d.get("bias"), d["w13"], d["w2"], w.k, w.scoring,
+                  w.n_group, w.topk_group, w.renormalize, w.scaling, block_m=block_m)
+    torch.cuda.synchronize()
+    tokens = sample_tokens(T, ntok, seed=seed)
+    ids_o, w_o, gap = oracle_router(oracle, w, d, T, tokens)
+    keep = gap > GAP_MIN
+    tokens, ids_o, w_o = tokens[keep], ids_o[keep], w_o[keep]
+    w13h, w2h, rid, En = compact_experts(d["w13"], d["w2"], ids_o)
+    ref = oracle.moe_ffn(host(d["hidden"])[tokens], "bf16", w13h, w2h, "bf16", len(tokens), w.H,
+                         w.F, En, w.k, rid, w_o)
+    got = y.float().cpu().numpy()[tokens]
+    err = rel_err(got, ref)
+    print(f"layer {name} T={T}: {len(tokens)} tokens compared, rel max err {err:.2e}")
+    assert len(tokens) > 0 and np.isfinite(got).all()
+    assert err <= LAYER_RTOL_BF16
+
+
+@pytest.mark.parametrize("name,T,ntok", [("toy", 16, 16), ("qwen3", 1, 1), ("qwen3", 64, 32),
+                                         ("qwen3", 512, 32), ("qwen3", 4096, 32),
+                                         ("dsv3", 1, 1), ("dsv3", 256, 12), ("dsv3", 4096, 12)])
+def test_layer_matches_oracle(name, T, ntok):
+    layer_case(name, T, ntok)
+
+
+def test_layer_zero_tokens():
+    w = W.WORKLOADS["toy"]
+    d = W.make_inputs(w, 1, device="cuda")
+    y = moe.layer(d["hidden"][:0], d["gate"], None, d["w13"], d["w2"], w.k)
+    assert y.shape == (0, w.H)
+
+
+def test_layer_is_deterministic():
+    w = W.WORKLOADS["qwen3"]
+    d = W.make_inputs(w, 512, seed=5, device="cuda")
+    a = moe.layer(d["hidden"], d["gate"], None, d["w13"], d["w2"], w.k)
+    b = moe.layer(d["hidden"], d["gate"], None, d["w13"], d["w2"], w.k)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+    ws = moe.default_workspace("cuda")
+    assert moe.read_device_error(ws.buf) == 0
