@@ -1,0 +1,529 @@
+"""Benchmark of the single-GPU MoE layer forward (router -> align -> GEMM1 +
+SwiGLU -> GEMM2 + weight -> finalize) on one GB300, one JSON line on stdout.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload qwen3] [--T 4096] [--no-sweep] [--no-cpu]
+
+A step is one pass of the whole hot path over one batch of T synthetic tokens
+(seeded inputs of the workload's shapes, random-init weights).  Each of the
+five kernels is captured in its own CUDA graph; a timed step replays the five
+graphs back to back with CUDA events between them on the launching stream, so
+the line carries the whole-step time and the dominant kernel's own time.
+Under torchrun every rank runs an independent replica (the layer has no
+collective); the step time is the maximum over ranks.
+
+--impl reference times the CPU oracle (the test-infrastructure reference of
+the method) on a bounded token sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = ("MoE layer µs/layer & tokens/s vs T (1..4096); router µs; "
+          "% HBM/tensor roofline")
+UNIT = "tokens/s"
+
+
+# --------------------------------------------------------------------------
+# peaks, clocks, distributed helpers
+# --------------------------------------------------------------------------
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        p = json.load(open(path))
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, period_ms: int = 100):
+        self.gpu_index = gpu_index
+        self.period_ms = period_ms
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", f"-lms={self.period_ms}"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self._t.join(timeout=5)
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def smi_index(local: int) -> str:
+    """nvidia-smi -i argument of this process's device (honours CUDA_VISIBLE_DEVICES)."""
+    cvd = os.environ.get("CUDA_VISIBLE_DEVICES", "").strip()
+    if cvd:
+        parts = [p.strip() for p in cvd.split(",") if p.strip()]
+        if local < len(parts):
+            return parts[local]
+    return str(local)
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def reduce_max(value: float, world: int, device=None) -> float:
+    """Maximum of a float over the ranks of the default process group."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int, device=None):
+    if world > 1:
+        import torch.distributed as dist
+        if device is not None and dist.get_backend() == "nccl":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+# --------------------------------------------------------------------------
+# algorithmic bytes / FLOPs (the method's own, padding and round trips apart)
+# --------------------------------------------------------------------------
+def work_model(w, T, touched, block_m, b_x=2, b_w=2, b_g=2):
+    H, E, k, F = w.H, w.E, w.k, w.F
+    cap = T * k + E * (block_m - 1)
+    st = {
+        "router": {"bytes": E * H * b_g + T * H * b_x + 8 * T * k, "flops": 2 * T * E * H},
+        "align": {"bytes": 4 * T * k + 4 * cap + 4 * math.ceil(cap / block_m), "flops": 0},
+        "gemm1": {"bytes": touched * 2 * F * H * b_w + T * H * b_x + T * k * F * 2,
+                  "flops": 2 * T * k * 2 * F * H},
+        "gemm2": {"bytes": touched * H * F * b_w + T * k * F * 2 + T * k * H * 2,
+                  "flops": 2 * T * k * H * F},
+        "finalize": {"bytes": T * k * H * 2 + T * H * 2, "flops": 0},
+    }
+    layer = {"bytes": touched * 3 * H * F * b_w + T * H * b_x + T * H * 2 + st["router"]["bytes"],
+             "flops": 6 * T * k * H * F + st["router"]["flops"]}
+    return st, layer
+
+
+def roofline_of(bytes_, flops, seconds, peaks):
+    t_hbm = bytes_ / (peaks["hbm_gbs"] * 1e9)
+    t_tc = flops / (peaks["bf16_tflops"] * 1e12)
+    if t_hbm >= t_tc:
+        ach = bytes_ / seconds / 1e9
+        return {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": ach / peaks["hbm_gbs"]}
+    ach = flops / seconds / 1e12
+    return {"bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+            "frac": ach / peaks["bf16_tflops"]}
+
+
+# --------------------------------------------------------------------------
+# CPU oracle leg
+# --------------------------------------------------------------------------
+def oracle_sample_step(w, d_host, T, tokens):
+    """One pass of the oracle's hot path over a token sample: router, align of
+    the sample's assignments, naive per-expert FFN and weighted sum."""
+    import numpy as np
+    import oracle
+    x_dt = "e4m3" if w.lowbit else "bf16"
+    g_dt = "f32" if w.lowbit else "bf16"
+    ids, wts, gap = oracle.router(d_host["hidden"], x_dt, d_host["gate"], g_dt,
+                                  d_host.get("bias"), T, w.H, w.E, w.k, w.scoring, w.n_group,
+                                  w.topk_group, w.renormalize, w.scaling,
+                                  x_scale=d_host.get("hidden_scale"), tokens=tokens)
+    from router_experts_gb300 import workloads as W
+    oracle.align(ids, len(tokens), w.k, w.E, W.block_m_for(T, w.k, w.E))
+    full_ids = np.zeros((T, w.k), np.int32)
+    full_w = np.zeros((T, w.k), np.float64)
+    full_ids[tokens] = ids
+    full_w[tokens] = wts
+    oracle.moe_ffn(d_host["hidden"], x_dt, d_host["w13"], d_host["w2"],
+                   "e2m1" if w.lowbit else "bf16", T, w.H, w.F, w.E, w.k, full_ids, full_w,
+                   x_scale=d_host.get("hidden_scale"), w13_scale=d_host.get("w13_scale"),
+                   w2_scale=d_host.get("w2_scale"), tokens=tokens)
+
+
+def host_inputs(d):
+    from router_experts_gb300 import workloads as W
+    out = {}
+    for k, v in d.items():
+        out[k] = v.cpu().numpy() if k == "bias" else W.to_host_raw(v)
+    return out
+
+
+def time_oracle(w, d_host, T, n_tokens, steps=1, seed=0):
+    import numpy as np
+    rng = np.random.default_rng(seed)
+    times = []
+    for s in range(steps):
+        tokens = np.sort(rng.choice(T, n_tokens, replace=False)).astype(np.int32)
+        t0 = time.perf_counter()
+        oracle_sample_step(w, d_host, T, tokens)
+        times.append(time.perf_counter() - t0)
+    return times
+
+
+# --------------------------------------------------------------------------
+# GPU leg
+# --------------------------------------------------------------------------
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    from router_experts_gb300 import build as B
+    from router_experts_gb300 import moe
+    from router_experts_gb300 import workloads as W
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    B.build()
+    moe.load()
+    peaks = load_peaks()
+    w = W.WORKLOADS[args.workload]
+    T = args.T
+    k, E, H, F = w.k, w.E, w.H, w.F
+    BM = moe.pick_block_m(T, k, E)
+    d = W.make_inputs(w, T, seed=args.seed, device=dev)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream(dev)
+
+    # ---- stage graphs (each holds exactly one kernel of the library) ----
+    ws = moe.Workspace(dev)
+    args_r = (d["hidden"], d["gate"], d.get("bias"), k, w.scoring, w.n_group, w.topk_group,
+              w.renormalize, w.scaling)
+    ids, wts = moe.router(*args_r, ws=ws)
+    s_ids, blk, npp = moe.align(ids, E, BM, ws=ws)
+    stage = moe.grouped_ffn(d["hidden"], d["w13"], d["w2"], k, BM, s_ids, blk, npp, wts, ws=ws)
+    y = moe.finalize(stage, T, k)
+    moe.layer(d["hidden"], d["gate"], d.get("bias"), d["w13"], d["w2"], k, w.scoring,
+              w.n_group, w.topk_group, w.renormalize, w.scaling, ws=ws)
+    torch.cuda.synchronize()
+    touched = int(torch.unique(ids).numel())
+    rows_per_expert = torch.bincount(ids.reshape(-1).long(), minlength=E)
+    npp_val = int(npp.item())
+
+    outs = {}
+    graphs = {}
+
+    def cap(name, fn):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            outs[name] = fn()
+        graphs[name] = g
+
+    cap("router", lambda: moe.router(*args_r, ws=ws, out=(ids, wts)))
+    cap("align", lambda: moe.align(ids, E, BM, ws=ws))
+    cap("gemm1", lambda: moe.expert_gemm1(d["hidden"], d["w13"], BM, s_ids, blk, npp, k, ws=ws))
+    inter = outs["gemm1"]
+    cap("gemm2", lambda: moe.expert_gemm2(inter, d["w2"], T, k, BM, s_ids, blk, npp, wts, ws=ws))
+    stage2 = outs["gemm2"]
+    cap("finalize", lambda: moe.finalize(stage2, T, k, out=y))
+    names = ["router", "align", "gemm1", "gemm2", "finalize"]
+    torch.cuda.synchronize()
+
+    weights_bytes = (d["w13"].numel() + d["w2"].numel()) * d["w13"].element_size()
+    l2_note = ("inputs larger than L2 (expert weights %.2f GB)" % (weights_bytes / 1e9)
+               if weights_bytes > 256e6 else "L2 flushed between steps")
+    flush = None if weights_bytes > 256e6 else torch.empty(512 << 20, dtype=torch.uint8,
+                                                           device=dev)
+
+    def step():
+        for n in names:
+            graphs[n].replay()
+
+    for _ in range(args.warmup):
+        if flush is not None:
+            flush.zero_()
+        step()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)] for _ in range(K)]
+    barrier(world, dev)
+    torch.cuda.synchronize()
+    with ClockSampler(smi_index(local)) as clk:
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        if flush is None:
+            t_start.record(stream)
+        total_steps_ms = 0.0
+        for i in range(K):
+            if flush is not None:
+                flush.zero_()
+            for j, n in enumerate(names):
+                ev[i][j].record(stream)
+                graphs[n].replay()
+            ev[i][len(names)].record(stream)
+        if flush is None:
+            t_end.record(stream)
+        torch.cuda.synchronize()
+    barrier(world, dev)
+    per_stage = {n: [] for n in names}
+    step_ms = []
+    for i in range(K):
+        for j, n in enumerate(names):
+            per_stage[n].append(ev[i][j].elapsed_time(ev[i][j + 1]))
+        step_ms.append(ev[i][0].elapsed_time(ev[i][len(names)]))
+    if flush is None:
+        total_ms = t_start.elapsed_time(t_end)
+    else:
+        total_ms = sum(step_ms)
+    total_ms = reduce_max(total_ms, world, dev)
+    ms_per_step = total_ms / K
+    value = world * T * K / (total_ms / 1e3)
+    stage_ms = {n: sum(v) / len(v) for n, v in per_stage.items()}
+    st_model, layer_model = work_model(w, T, touched, BM)
+    dom = max(names, key=lambda n: stage_ms[n])
+    roof = roofline_of(st_model[dom]["bytes"], st_model[dom]["flops"], stage_ms[dom] / 1e3, peaks)
+    roof["kernel"] = {"router": "router_kernel", "align": "align_kernel",
+                      "gemm1": "ffn_gemm_kernel<0,%d>" % BM, "gemm2": "ffn_gemm_kernel<1,%d>" % BM,
+                      "finalize": "finalize_kernel"}[dom]
+    roof["traffic"] = None
+    roof["peak_source"] = peaks["source"] + " (burst)"
+    layer_roof = roofline_of(layer_model["bytes"], layer_model["flops"], ms_per_step / 1e3, peaks)
+
+    # ---- sweep over T (L2 flushed before each replay) ----
+    sweep = {}
+    if not args.no_sweep and rank == 0:
+        fl = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+        for Ts in w.Ts:
+            if Ts > T:
+                continue
+            xs = d["hidden"][:Ts].contiguous()
+            g = torch.cuda.CUDAGraph()
+            moe.layer(xs, d["gate"], d.get("bias"), d["w13"], d["w2"], k, w.scoring, w.n_group,
+                      w.topk_group, w.renormalize, w.scaling, ws=ws)
+            with torch.cuda.graph(g):
+                moe.layer(xs, d["gate"], d.get("bias"), d["w13"], d["w2"], k, w.scoring,
+                          w.n_group, w.topk_group, w.renormalize, w.scaling, ws=ws)
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr):
+                moe.router(xs, d["gate"], d.get("bias"), k, w.scoring, w.n_group, w.topk_group,
+                           w.renormalize, w.scaling, ws=ws)
+            res = {}
+            for key, gg in (("layer", g), ("router", gr)):
+                ts = []
+                for _ in range(25):
+                    fl.zero_()
+                    a = torch.cuda.Event(enable_timing=True)
+                    b = torch.cuda.Event(enable_timing=True)
+                    a.record(stream)
+                    gg.replay()
+                    b.record(stream)
+                    torch.cuda.synchronize()
+                    ts.append(a.elapsed_time(b) * 1e3)
+                res[key] = statistics.median(ts[3:])
+            ids_s, _ = moe.router(xs, d["gate"], d.get("bias"), k, w.scoring, w.n_group,
+                                  w.topk_group, w.renormalize, w.scaling, ws=ws)
+            tch = int(torch.unique(ids_s).numel())
+            _, lm = work_model(w, Ts, tch, moe.pick_block_m(Ts, k, E))
+            lr = roofline_of(lm["bytes"], lm["flops"], res["layer"] / 1e6, peaks)
+            sweep[str(Ts)] = {"us_per_layer": round(res["layer"], 2),
+                              "tokens_per_s": round(Ts / (res["layer"] / 1e6), 1),
+                              "router_us": round(res["router"], 2), "touched_experts": tch,
+                              "block_m": moe.pick_block_m(Ts, k, E),
+                              "roofline": {"bound": lr["bound"], "frac": round(lr["frac"], 4)}}
+            del g, gr
+        del fl
+
+    # ---- end to end through the public API, host buffers ----
+    x_host = d["hidden"].cpu().pin_memory()
+    y_host = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
+    x_dev = torch.empty_like(d["hidden"])
+    y_dev = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    K2 = max(3, min(K, 50))
+    for _ in range(2):
+        x_dev.copy_(x_host, non_blocking=True)
+        moe.layer(x_dev, d["gate"], d.get("bias"), d["w13"], d["w2"], k, w.scoring, w.n_group,
+                  w.topk_group, w.renormalize, w.scaling, ws=ws, out=y_dev)
+        y_host.copy_(y_dev, non_blocking=True)
+    torch.cuda.synchronize()
+    barrier(world, dev)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(K2):
+        x_dev.copy_(x_host, non_blocking=True)
+        moe.layer(x_dev, d["gate"], d.get("bias"), d["w13"], d["w2"], k, w.scoring, w.n_group,
+                  w.topk_group, w.renormalize, w.scaling, ws=ws, out=y_dev)
+        y_host.copy_(y_dev, non_blocking=True)
+    b.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = reduce_max(a.elapsed_time(b), world, dev)
+    e2e = {"value": round(world * T * K2 / (e2e_ms / 1e3), 1), "unit": UNIT,
+           "h2d_bytes_per_step": T * H * 2, "d2h_bytes_per_step": T * H * 2}
+    code = moe.read_device_error(ws.buf)
+
+    # ---- CPU oracle baseline (rank 0, N = 1 only) ----
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        import oracle
+        oracle.build()
+        dh = host_inputs(d)
+        n_tok = args.cpu_tokens
+        times = time_oracle(w, dh, T, n_tok, steps=1, seed=1)
+        cpu = {"value": round(n_tok / times[0], 3), "unit": UNIT, "cores": oracle.num_threads(),
+               "kind": "oracle",
+               "sample": f"{n_tok} of the {T} tokens (router, align of their assignments, "
+                         f"naive per-expert FFN, combine), one pass, {times[0]:.1f} s"}
+
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{w.name} MoE layer forward (H={H}, E={E}, k={k}, F={F}, "
+                               f"{w.scoring}{', groups %d/%d' % (w.n_group, w.topk_group) if w.n_group > 1 else ''}), "
+                               f"T={T} tokens, BLOCK_M={BM}, random-init weights",
+                   "T": T, "block_m": BM, "touched_experts": touched,
+                   "max_rows_per_expert": int(rows_per_expert.max().item()),
+                   "padded_rows": npp_val, "l2": l2_note,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": {k2: (round(v, 4) if isinstance(v, float) else v) for k2, v in roof.items()},
+        "layer_roofline": {k2: (round(v, 4) if isinstance(v, float) else v)
+                           for k2, v in layer_roof.items()},
+        "stage_us": {n: round(v * 1e3, 2) for n, v in stage_ms.items()},
+        "sweep": sweep,
+        "e2e": e2e,
+        "gpu_launches": len(names) * K,
+        "cpu_baseline": cpu,
+        "device_error_word": code,
+    }
+    clocks = clk.summary()
+    line["clocks"] = clocks
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_reference(args):
+    """The CPU oracle as the reference arm, on a bounded token sample."""
+    world, rank, local = dist_env()
+    if rank != 0:
+        return
+    import torch
+
+    import oracle
+    from router_experts_gb300 import workloads as W
+    oracle.build()
+    w = W.WORKLOADS[args.workload]
+    T = args.T
+    d = W.make_inputs(w, T, seed=args.seed, device="cpu")
+    dh = host_inputs(d)
+    # size the per-step sample so that warm-up + K steps take about two minutes
+    t1 = time_oracle(w, dh, T, 1, steps=1, seed=100)[0]
+    budget = 120.0 / max(1, args.steps + 1)
+    n_tok = int(max(1, min(args.ref_tokens, budget // max(t1, 1e-6))))
+    time_oracle(w, dh, T, n_tok, steps=1, seed=101)
+    times = time_oracle(w, dh, T, n_tok, steps=args.steps, seed=0)
+    tot = sum(times)
+    value = n_tok * len(times) / tot
+    sample = (f"{n_tok} of the {T} tokens per step (router, align of their assignments, "
+              f"naive per-expert FFN, combine)")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(tot / len(times) * 1e3, 2), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{w.name} MoE layer forward (H={w.H}, E={w.E}, k={w.k}, "
+                               f"F={w.F}), T={T} tokens, random-init weights", "T": T},
+        "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": oracle.num_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="qwen3")
+    ap.add_argument("--T", type=int, default=4096)
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-tokens", type=int, default=256)
+    ap.add_argument("--ref-tokens", type=int, default=32)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        if "--steps" not in (argv if argv is not None else sys.argv):
+            args.steps = 5
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -39,7 +39,7 @@ def compact_experts(w13, w2, ids_rows):
     idx = torch.as_tensor(used, dtype=torch.long, device=w13.device)
     w13h = host(w13.index_select(0, idx))
     w2h = host(w2.index_select(0, idx))
-    new_ids = np.vectorize(lambda e: remap[int(e)])(ids_rows).astype(np.int32)
+    new_ids = np.array([[remap[int(e)] for e in r] for r in ids_rows], dtype=np.int32).reshape(ids_rows.shape)
     return w13h, w2h, new_ids, len(used)
 
 

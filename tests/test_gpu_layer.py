@@ -17,13 +17,17 @@ pytestmark = pytest.mark.gpu
 
 def layer_case(name, T, ntok, block_m=0, seed=0):
     w = W.WORKLOADS[name]
-    d = W.make_inputs(w, T, seed=seed, device="cuda")
+    # small batches may have no token clear of the 1e-4 cut: try further seeds
+    for seed in range(seed, seed + 10):
+        d = W.make_inputs(w, T, seed=seed, device="cuda")
+        tokens = sample_tokens(T, ntok, seed=seed)
+        ids_o, w_o, gap = oracle_router(oracle, w, d, T, tokens)
+        keep = gap > GAP_MIN
+        if keep.any():
+            break
     y = moe.layer(d["hidden"], d["gate"], d.get("bias"), d["w13"], d["w2"], w.k, w.scoring,
                   w.n_group, w.topk_group, w.renormalize, w.scaling, block_m=block_m)
     torch.cuda.synchronize()
-    tokens = sample_tokens(T, ntok, seed=seed)
-    ids_o, w_o, gap = oracle_router(oracle, w, d, T, tokens)
-    keep = gap > GAP_MIN
     tokens, ids_o, w_o = tokens[keep], ids_o[keep], w_o[keep]
     w13h, w2h, rid, En = compact_experts(d["w13"], d["w2"], ids_o)
     ref = oracle.moe_ffn(host(d["hidden"])[tokens], "bf16", w13h, w2h, "bf16", len(tokens), w.H,
