@@ -91,6 +91,42 @@ int moe_router(const void* hidden, int hidden_dt, const uint8_t* hidden_scale, c
                float* topk_weights, void* ws, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * moe_router_noalloc -- the router for callers that cannot allocate device
+ * memory.  (No counterpart on the pages: it exists for this library's users.)
+ *
+ * Some callers cannot call cudaMalloc or any other allocator: code embedded
+ * in a host framework that owns all device memory, plugins whose process
+ * memory pool must not grow, or hosts that forbid allocation after start-up.
+ * moe_router needs a caller-allocated workspace; this variant instead keeps
+ * its scratch (partial logits and tickets) in one fixed array of device
+ * memory that belongs to the library (a file-scope static __device__ array),
+ * so the caller passes only the inputs and the outputs, exactly as for
+ * moe_router, and nothing is allocated or freed.
+ *
+ *   - Same arguments, rules and results as moe_router, without ws/ws_bytes.
+ *   - Limit: the partial logits of one call, KS * T * E * 4 bytes with the
+ *     K-split count KS the router picks (16 for a few tokens, 1 for thousands),
+ *     must fit in MOE_ROUTER_NOALLOC_MAX_LOGIT_BYTES (8 MiB), and
+ *     T <= 262,144.  Larger problems are rejected with MOE_ERR_ARG before
+ *     anything is launched (e.g. T = 4,096 fits for every E <= 512;
+ *     T = 8,192 with E = 512 does not).
+ *   - The array (about 8.3 MiB) exists on every GPU that loads the library,
+ *     until the process exits.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - Every call shares the one array and leaves its contents behind; each
+ *     call clears the tickets it uses before launching.  Calls that overlap in
+ *     time on the GPU (different streams, or several host threads) race on
+ *     the array and produce wrong results: serialise them.
+ * ------------------------------------------------------------------------- */
+#define MOE_ROUTER_NOALLOC_MAX_LOGIT_BYTES (8u << 20)
+int moe_router_noalloc(const void* hidden, int hidden_dt, const uint8_t* hidden_scale,
+                       const void* gate, int gate_dt, const float* bias, int T, int H, int E,
+                       int k, int scoring, int n_group, int topk_group, int renormalize,
+                       float scaling, int32_t* topk_ids, float* topk_weights, void* stream);
+
+/* ---------------------------------------------------------------------------
  * Align (moe_align_block_size).  [P3] "Alignment: making ragged routing
  * tileable" (count per expert, round up to block_m, exclusive prefix sum,
  * sorted assignment ids with the sentinel T*k for padding, expert of every

@@ -1,0 +1,84 @@
+"""moe_router_noalloc: the router for callers that cannot allocate device memory.
+
+Callers embedded in a framework that owns all device memory (or forbidden to
+allocate after start-up) cannot hand the router a workspace.  This entry point
+keeps its scratch in a fixed array inside the library instead.  These tests
+call it through the C ABI and compare its ids and weights with moe_router's
+(the entry point with a caller workspace) on two calls in a row, with other
+shapes in between, and check that oversized problems are refused.  The file is
+collected last on purpose."""
+import ctypes
+
+import pytest
+import torch
+
+from router_experts_gb300 import moe
+from router_experts_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+WEIGHT_ATOL = 1e-5
+
+
+def noalloc_fn():
+    lib = moe.load()
+    fn = lib.moe_router_noalloc
+    P, I = ctypes.c_void_p, ctypes.c_int
+    fn.restype = I
+    fn.argtypes = [P, I, P, P, I, P, I, I, I, I, I, I, I, I, ctypes.c_float, P, P, P]
+    return fn
+
+
+def ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def call_noalloc(fn, w, d, T):
+    ids = torch.empty((T, w.k), dtype=torch.int32, device="cuda")
+    wts = torch.empty((T, w.k), dtype=torch.float32, device="cuda")
+    x_dt = moe.DT_E4M3 if w.lowbit else moe.DT_BF16
+    g_dt = moe.DT_F32 if w.lowbit else moe.DT_BF16
+    rc = fn(ptr(d["hidden"]), x_dt, ptr(d.get("hidden_scale")), ptr(d["gate"]), g_dt,
+            ptr(d.get("bias")), T, w.H, w.E, w.k, moe.SOFTMAX if w.scoring == "softmax" else
+            moe.SIGMOID, w.n_group, w.topk_group, int(w.renormalize), w.scaling, ptr(ids),
+            ptr(wts), ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert rc == moe.MOE_OK, rc
+    return ids, wts
+
+
+def reference(w, d):
+    ws = moe.Workspace("cuda")
+    return moe.router(d["hidden"], d["gate"], d.get("bias"), w.k, w.scoring, w.n_group,
+                      w.topk_group, w.renormalize, w.scaling, hidden_scale=d.get("hidden_scale"),
+                      ws=ws)
+
+
+@pytest.mark.parametrize("seq", [[("glm", 64), ("glm", 64)],
+                                 [("qwen3", 1), ("dsv3", 4096), ("qwen3", 1)],
+                                 [("v4lo", 512), ("toy", 16), ("v4lo", 512)]])
+def test_noalloc_matches_router_on_consecutive_calls(seq):
+    fn = noalloc_fn()
+    for name, T in seq:
+        w = W.WORKLOADS[name]
+        d = W.make_inputs(w, T, seed=11, device="cuda", experts=False)
+        ref_ids, ref_w = reference(w, d)
+        ids, wts = call_noalloc(fn, w, d, T)
+        torch.cuda.synchronize()
+        assert torch.equal(ids, ref_ids), name
+        assert (wts - ref_w).abs().max().item() <= WEIGHT_ATOL
+
+
+def test_noalloc_rejects_sizes_beyond_its_array():
+    fn = noalloc_fn()
+    # 8192 tokens x 512 experts x 4 bytes = 16 MiB of partial logits > 8 MiB.
+    # Every buffer has its full size, so even a wrongly accepted call would
+    # only run a correct router.
+    E, H, k, T = 512, 4096, 8, 8192
+    x = torch.zeros((T, H), dtype=torch.bfloat16, device="cuda")
+    g = torch.zeros((E, H), dtype=torch.bfloat16, device="cuda")
+    ids = torch.zeros((T, k), dtype=torch.int32, device="cuda")
+    wts = torch.zeros((T, k), dtype=torch.float32, device="cuda")
+    rc = fn(ptr(x), moe.DT_BF16, None, ptr(g), moe.DT_BF16, None, T, H, E, k, moe.SOFTMAX, 1, 1,
+            1, 1.0, ptr(ids), ptr(wts), None)
+    torch.cuda.synchronize()
+    assert rc == moe.MOE_ERR_ARG
