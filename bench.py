@@ -254,37 +254,46 @@ def run_ours(args):
 
     # ---- stage graphs (each holds exactly one kernel of the library) ----
     ws = moe.Workspace(dev)
-    args_r = (d["hidden"], d["gate"], d.get("bias"), k, w.scoring, w.n_group, w.topk_group,
-              w.renormalize, w.scaling)
-    ids, wts = moe.router(*args_r, ws=ws)
-    s_ids, blk, npp = moe.align(ids, E, BM, ws=ws)
-    stage = moe.grouped_ffn(d["hidden"], d["w13"], d["w2"], k, BM, s_ids, blk, npp, wts, ws=ws)
-    y = moe.finalize(stage, T, k)
-    moe.layer(d["hidden"], d["gate"], d.get("bias"), d["w13"], d["w2"], k, w.scoring,
-              w.n_group, w.topk_group, w.renormalize, w.scaling, ws=ws)
-    torch.cuda.synchronize()
-    touched = int(torch.unique(ids).numel())
-    rows_per_expert = torch.bincount(ids.reshape(-1).long(), minlength=E)
-    npp_val = int(npp.item())
-
-    outs = {}
-    graphs = {}
-
-    def cap(name, fn):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            outs[name] = fn()
-        graphs[name] = g
-
-    cap("router", lambda: moe.router(*args_r, ws=ws, out=(ids, wts)))
-    cap("align", lambda: moe.align(ids, E, BM, ws=ws))
-    cap("gemm1", lambda: moe.expert_gemm1(d["hidden"], d["w13"], BM, s_ids, blk, npp, k, ws=ws))
-    inter = outs["gemm1"]
-    cap("gemm2", lambda: moe.expert_gemm2(inter, d["w2"], T, k, BM, s_ids, blk, npp, wts, ws=ws))
-    stage2 = outs["gemm2"]
-    cap("finalize", lambda: moe.finalize(stage2, T, k, out=y))
     names = ["router", "align", "gemm1", "gemm2", "finalize"]
-    torch.cuda.synchronize()
+
+    def stage_graphs(x):
+        """One CUDA graph per kernel for the batch x; returns graphs + routing facts."""
+        Tn = x.shape[0]
+        bm = moe.pick_block_m(Tn, k, E)
+        a_r = (x, d["gate"], d.get("bias"), k, w.scoring, w.n_group, w.topk_group,
+               w.renormalize, w.scaling)
+        ids, wts = moe.router(*a_r, ws=ws)
+        s_ids, blk, npp = moe.align(ids, E, bm, ws=ws)
+        inter = moe.expert_gemm1(x, d["w13"], bm, s_ids, blk, npp, k, ws=ws)
+        st = moe.expert_gemm2(inter, d["w2"], Tn, k, bm, s_ids, blk, npp, wts, ws=ws)
+        y = moe.finalize(st, Tn, k)
+        torch.cuda.synchronize()
+        gs, outs = {}, {}
+
+        def cap(name, fn):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                outs[name] = fn()
+            gs[name] = g
+
+        cap("router", lambda: moe.router(*a_r, ws=ws, out=(ids, wts)))
+        cap("align", lambda: moe.align(ids, E, bm, ws=ws))
+        s2, b2, n2 = outs["align"]
+        cap("gemm1", lambda: moe.expert_gemm1(x, d["w13"], bm, s2, b2, n2, k, ws=ws))
+        i2 = outs["gemm1"]
+        cap("gemm2", lambda: moe.expert_gemm2(i2, d["w2"], Tn, k, bm, s2, b2, n2, wts, ws=ws))
+        st2 = outs["gemm2"]
+        cap("finalize", lambda: moe.finalize(st2, Tn, k, out=y))
+        for n in names:
+            gs[n].replay()
+        torch.cuda.synchronize()
+        facts = {"touched": int(torch.unique(ids).numel()), "block_m": bm,
+                 "max_rows": int(torch.bincount(ids.reshape(-1).long(), minlength=E).max()),
+                 "padded_rows": int(n2.item())}
+        return gs, facts, outs
+
+    graphs, facts, keep_alive = stage_graphs(d["hidden"])
+    BM, touched = facts["block_m"], facts["touched"]
 
     weights_bytes = (d["w13"].numel() + d["w2"].numel()) * d["w13"].element_size()
     l2_note = ("inputs larger than L2 (expert weights %.2f GB)" % (weights_bytes / 1e9)
@@ -311,7 +320,6 @@ def run_ours(args):
         t_end = torch.cuda.Event(enable_timing=True)
         if flush is None:
             t_start.record(stream)
-        total_steps_ms = 0.0
         for i in range(K):
             if flush is not None:
                 flush.zero_()
@@ -346,49 +354,65 @@ def run_ours(args):
     roof["traffic"] = None
     roof["peak_source"] = peaks["source"] + " (burst)"
     layer_roof = roofline_of(layer_model["bytes"], layer_model["flops"], ms_per_step / 1e3, peaks)
+    del graphs, keep_alive
 
-    # ---- sweep over T (L2 flushed before each replay) ----
+    # ---- sweep over T: per-kernel times, L2 flushed before each replay ----
     sweep = {}
     if not args.no_sweep and rank == 0:
         fl = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
         for Ts in w.Ts:
-            if Ts > T:
+            if Ts >= T:
                 continue
             xs = d["hidden"][:Ts].contiguous()
-            g = torch.cuda.CUDAGraph()
+            gs, fs, ka = stage_graphs(xs)
+            times = {n: [] for n in names}
+            for it in range(25):
+                fl.zero_()
+                evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)]
+                for j, n in enumerate(names):
+                    evs[j].record(stream)
+                    gs[n].replay()
+                evs[-1].record(stream)
+                torch.cuda.synchronize()
+                if it >= 3:
+                    for j, n in enumerate(names):
+                        times[n].append(evs[j].elapsed_time(evs[j + 1]) * 1e3)
+            us = {n: statistics.median(v) for n, v in times.items()}
+            # the layer as a user runs it: one graph holding the five kernels
+            lg = torch.cuda.CUDAGraph()
             moe.layer(xs, d["gate"], d.get("bias"), d["w13"], d["w2"], k, w.scoring, w.n_group,
                       w.topk_group, w.renormalize, w.scaling, ws=ws)
-            with torch.cuda.graph(g):
+            with torch.cuda.graph(lg):
                 moe.layer(xs, d["gate"], d.get("bias"), d["w13"], d["w2"], k, w.scoring,
                           w.n_group, w.topk_group, w.renormalize, w.scaling, ws=ws)
-            gr = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(gr):
-                moe.router(xs, d["gate"], d.get("bias"), k, w.scoring, w.n_group, w.topk_group,
-                           w.renormalize, w.scaling, ws=ws)
-            res = {}
-            for key, gg in (("layer", g), ("router", gr)):
-                ts = []
-                for _ in range(25):
-                    fl.zero_()
-                    a = torch.cuda.Event(enable_timing=True)
-                    b = torch.cuda.Event(enable_timing=True)
-                    a.record(stream)
-                    gg.replay()
-                    b.record(stream)
-                    torch.cuda.synchronize()
-                    ts.append(a.elapsed_time(b) * 1e3)
-                res[key] = statistics.median(ts[3:])
-            ids_s, _ = moe.router(xs, d["gate"], d.get("bias"), k, w.scoring, w.n_group,
-                                  w.topk_group, w.renormalize, w.scaling, ws=ws)
-            tch = int(torch.unique(ids_s).numel())
-            _, lm = work_model(w, Ts, tch, moe.pick_block_m(Ts, k, E))
-            lr = roofline_of(lm["bytes"], lm["flops"], res["layer"] / 1e6, peaks)
-            sweep[str(Ts)] = {"us_per_layer": round(res["layer"], 2),
-                              "tokens_per_s": round(Ts / (res["layer"] / 1e6), 1),
-                              "router_us": round(res["router"], 2), "touched_experts": tch,
-                              "block_m": moe.pick_block_m(Ts, k, E),
+            lt = []
+            for it in range(25):
+                fl.zero_()
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                lg.replay()
+                e1.record(stream)
+                torch.cuda.synchronize()
+                if it >= 3:
+                    lt.append(e0.elapsed_time(e1) * 1e3)
+            tot = statistics.median(lt)
+            del lg
+            sm_, lm = work_model(w, Ts, fs["touched"], fs["block_m"])
+            lr = roofline_of(lm["bytes"], lm["flops"], tot / 1e6, peaks)
+            sweep[str(Ts)] = {"us_per_layer": round(tot, 2),
+                              "tokens_per_s": round(Ts / (tot / 1e6), 1),
+                              "stage_us": {n: round(v, 2) for n, v in us.items()},
+                              "stage_note": "each kernel as its own graph (incl. launch gaps)",
+                              "touched_experts": fs["touched"], "block_m": fs["block_m"],
                               "roofline": {"bound": lr["bound"], "frac": round(lr["frac"], 4)}}
-            del g, gr
+            del gs, ka
+        sweep[str(T)] = {"us_per_layer": round(ms_per_step * 1e3, 2),
+                         "tokens_per_s": round(T / (ms_per_step / 1e3), 1),
+                         "stage_us": {n: round(v * 1e3, 2) for n, v in stage_ms.items()},
+                         "touched_experts": touched, "block_m": BM,
+                         "roofline": {"bound": layer_roof["bound"],
+                                      "frac": round(layer_roof["frac"], 4)}}
         del fl
 
     # ---- end to end through the public API, host buffers ----
@@ -440,8 +464,8 @@ def run_ours(args):
                                f"{w.scoring}{', groups %d/%d' % (w.n_group, w.topk_group) if w.n_group > 1 else ''}), "
                                f"T={T} tokens, BLOCK_M={BM}, random-init weights",
                    "T": T, "block_m": BM, "touched_experts": touched,
-                   "max_rows_per_expert": int(rows_per_expert.max().item()),
-                   "padded_rows": npp_val, "l2": l2_note,
+                   "max_rows_per_expert": facts["max_rows"],
+                   "padded_rows": facts["padded_rows"], "l2": l2_note,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": {k2: (round(v, 4) if isinstance(v, float) else v) for k2, v in roof.items()},
         "layer_roofline": {k2: (round(v, 4) if isinstance(v, float) else v)

@@ -10,13 +10,16 @@
 // them in ascending assignment id, so its output is unique.
 //
 // One CTA of 1024 threads.  Warp w owns a contiguous segment of assignments.
-// Pass 1: per 32-assignment chunk, __match_any_sync groups lanes with the same
-// expert and the group leader adds the group size to the warp's shared-memory
-// histogram row.  Then, per expert, an exclusive scan over the 32 warp rows
+// Pass 1 counts the segment into the warp's shared-memory histogram row.  Then, per expert, an exclusive scan over the 32 warp rows
 // gives each warp its base inside the expert, and a block-wide exclusive scan
 // of the padded counts gives the experts' starts.  Pass 2 re-walks the segment
-// in order: position = start[e] + warp base + rank among equal lanes to the
-// left; the leader advances the warp's running base.
+// in 32-assignment chunks: one ballot per id bit finds the lanes holding the
+// same expert, position = start[e] + warp base + rank among those lanes to the
+// left, and the group leader advances the warp's running base.  When the
+// problem fits in shared memory, pass 2 places into a compact shared-memory
+// array and a final sweep writes sorted_ids (pads and tail included) and the
+// block table with coalesced stores; a single SM issuing tens of thousands of
+// scattered 4-byte stores is otherwise the bottleneck.
 #include "moe_common.cuh"
 #include "moe_internal.h"
 
@@ -36,6 +39,50 @@ MOE_DEV int warp_incl_scan(int v) {
   return v;
 }
 
+// Mask of the lanes holding the same expert id as this lane (0 for an invalid
+// lane), from one ballot per id bit: the lanes that agree with this lane on
+// every bit.
+MOE_DEV unsigned match_lanes(int e, bool valid, int nbits) {
+  unsigned m = __ballot_sync(0xffffffffu, valid);
+  for (int b = 0; b < nbits; ++b) {
+    const bool bit = (e >> b) & 1;
+    const unsigned v = __ballot_sync(0xffffffffu, bit);
+    m &= bit ? v : ~v;
+  }
+  return valid ? m : 0u;
+}
+
+// Expert id of assignment a: from the shared-memory copy when the ids were
+// staged (STAGED), else from global memory.  Invalid ids read as -1.
+template <bool STAGED>
+MOE_DEV int load_id(const int32_t* __restrict__ ids, const uint16_t* sid, int a, int E) {
+  if constexpr (STAGED) {
+    const int v = sid[a];
+    return v == 0xFFFF ? -1 : v;
+  } else {
+    const int v = __ldg(ids + a);
+    return (v >= 0 && v < E) ? v : -1;
+  }
+}
+
+// Shared-memory layout of the compact (STAGED) variant, in 32-bit words:
+//   cnt[32][E] | tot[E] | start[E] | cstart[E] | wsum[32] | blk[nbc]
+//   | sid[n] (uint16) | out[n] (uint16)
+struct AlignSmem {
+  size_t words, bytes;
+};
+inline AlignSmem align_smem(int n, int E, long long nbc) {
+  AlignSmem m;
+  m.words = 32 * static_cast<size_t>(E) + 3 * static_cast<size_t>(E) + 32 + nbc;
+  m.bytes = m.words * 4 + align_up(static_cast<size_t>(n) * 2, 16) * 2;
+  return m;
+}
+
+// STAGED: ids staged in shared memory (16-bit) and the sorted assignment ids
+// built in shared memory first, so every global store is coalesced.
+// Otherwise (problems too large for shared memory): ids read from global
+// memory and placed with scattered stores.
+template <bool STAGED>
 __global__ void __launch_bounds__(kAlignThreads) align_kernel(const int32_t* __restrict__ ids,
                                                               int n, int E, int BM,
                                                               int32_t* __restrict__ sorted_ids,
@@ -47,27 +94,50 @@ __global__ void __launch_bounds__(kAlignThreads) align_kernel(const int32_t* __r
   int* cnt = sm;              // [32][E]: warp histogram, then running positions
   int* tot = cnt + 32 * E;    // [E] assignments per expert
   int* start = tot + E;       // [E] padded start of each expert
-  int* wsum = start + E;      // [32]
+  int* cstart = start + E;    // [E] start of each expert among the real assignments
+  int* wsum = cstart + E;     // [32]
+  int* blk = wsum + 32;       // [nblocks_cap] (STAGED) expert of each block
+  uint16_t* sid = reinterpret_cast<uint16_t*>(blk + (STAGED ? nblocks_cap : 0));
+  uint16_t* out = sid + align_up(static_cast<size_t>(n), 8);  // [n] (STAGED)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const unsigned lt_mask = (1u << lane) - 1u;
+  const int nbits = 32 - __clz(max(E - 1, 1));
 
   for (int i = tid; i < 32 * E; i += kAlignThreads) cnt[i] = 0;
+  bool bad = false;
+  if constexpr (STAGED) {
+    // coalesced copy of the ids into shared memory as 16-bit values; each
+    // thread issues several independent loads before it stores
+    constexpr int kU = 8;
+    for (int a0s = tid; a0s < n; a0s += kAlignThreads * kU) {
+      int v[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int a = a0s + u * kAlignThreads;
+        v[u] = (a < n) ? __ldg(ids + a) : 0;
+      }
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int a = a0s + u * kAlignThreads;
+        if (a < n) {
+          const bool ok = v[u] >= 0 && v[u] < E;
+          bad |= !ok;
+          sid[a] = ok ? static_cast<uint16_t>(v[u]) : static_cast<uint16_t>(0xFFFF);
+        }
+      }
+    }
+  }
   __syncthreads();
 
   const int per_warp = ((n + 31) / 32 + 31) / 32 * 32;
   const int a0 = warp * per_warp;
   const int a1 = min(n, a0 + per_warp);
 
-  bool bad = false;
-  for (int base = a0; base < a1; base += 32) {
-    const int a = base + lane;
-    const bool act = a < a1;
-    const int e = act ? __ldg(ids + a) : -1;
-    const bool ok = act && e >= 0 && e < E;
-    bad |= act && !ok;
-    const int key = ok ? e : (0x40000000 | lane);  // invalid lanes match nobody
-    const unsigned m = __match_any_sync(0xffffffffu, key);
-    if (ok && lane == __ffs(m) - 1) cnt[warp * E + e] += __popc(m);
+  // pass 1: per-warp histogram (shared-memory atomics on the warp's own row)
+  for (int a = a0 + lane; a < a1; a += 32) {
+    const int e = load_id<STAGED>(ids, sid, a, E);
+    if (e >= 0) atomicAdd(&cnt[warp * E + e], 1);
+    else if constexpr (!STAGED) bad = true;
   }
   if (bad) raise_error(err, kErrBadExpert);
   __syncthreads();
@@ -83,45 +153,101 @@ __global__ void __launch_bounds__(kAlignThreads) align_kernel(const int32_t* __r
   }
   __syncthreads();
 
-  // exclusive scan of the padded counts (E <= 1024: one expert per thread)
-  const int pad = (tid < E) ? (tot[tid] + BM - 1) / BM * BM : 0;
+  // exclusive scans over experts (E <= 1024: one expert per thread) of the
+  // padded counts (starts in sorted_ids) and of the real counts (compact starts)
+  const int cnt_e = (tid < E) ? tot[tid] : 0;
+  const int pad = (cnt_e + BM - 1) / BM * BM;
   const int incl = warp_incl_scan(pad);
+  const int cincl = warp_incl_scan(cnt_e);
   if (lane == 31) wsum[warp] = incl;
   __syncthreads();
   if (warp == 0) wsum[lane] = warp_incl_scan(wsum[lane]);
   __syncthreads();
   const int excl = incl - pad + (warp > 0 ? wsum[warp - 1] : 0);
-  if (tid < E) start[tid] = excl;
   const int total = wsum[31];
   __syncthreads();
-  for (int i = tid; i < 32 * E; i += kAlignThreads) cnt[i] += start[i % E];
+  if (lane == 31) wsum[warp] = cincl;
+  __syncthreads();
+  if (warp == 0) wsum[lane] = warp_incl_scan(wsum[lane]);
+  __syncthreads();
+  const int cexcl = cincl - cnt_e + (warp > 0 ? wsum[warp - 1] : 0);
+  if (tid < E) {
+    start[tid] = excl;
+    cstart[tid] = cexcl;
+  }
+  __syncthreads();
+  // warp bases: compact positions (STAGED) or positions in sorted_ids
+  for (int i = tid; i < 32 * E; i += kAlignThreads)
+    cnt[i] += STAGED ? cstart[i % E] : start[i % E];
+  if constexpr (STAGED) {
+    for (int e = tid; e < E; e += kAlignThreads) {
+      const int s = start[e], p = (tot[e] + BM - 1) / BM * BM;
+      for (int b = s / BM; b < (s + p) / BM; ++b) blk[b] = e;
+    }
+  }
   __syncthreads();
 
-  for (int base = a0; base < a1; base += 32) {
-    const int a = base + lane;
-    const bool act = a < a1;
-    const int e = act ? __ldg(ids + a) : -1;
-    const bool ok = act && e >= 0 && e < E;
-    const int key = ok ? e : (0x40000000 | lane);
-    const unsigned m = __match_any_sync(0xffffffffu, key);
-    const int pos0 = ok ? cnt[warp * E + e] : 0;
-    __syncwarp();
-    if (ok) {
-      sorted_ids[pos0 + __popc(m & lt_mask)] = a;
-      if (lane == __ffs(m) - 1) cnt[warp * E + e] = pos0 + __popc(m);
+  // pass 2: place in order.  The lane masks of a group of chunks do not depend
+  // on each other, so they are computed first; the running positions are then
+  // advanced chunk by chunk.
+  constexpr int kGroup = 8;
+  for (int g0 = a0; g0 < a1; g0 += 32 * kGroup) {
+    const int nch = min(kGroup, (a1 - g0 + 31) / 32);
+    int ev[kGroup];
+    unsigned mv[kGroup];
+#pragma unroll
+    for (int c = 0; c < kGroup; ++c) {
+      if (c < nch) {
+        const int a = g0 + 32 * c + lane;
+        ev[c] = (a < a1) ? load_id<STAGED>(ids, sid, a, E) : -1;
+        mv[c] = match_lanes(ev[c], ev[c] >= 0, nbits);
+      }
     }
-    __syncwarp();
+#pragma unroll
+    for (int c = 0; c < kGroup; ++c) {
+      if (c < nch) {
+        const int a = g0 + 32 * c + lane;
+        const int e = ev[c];
+        const unsigned m = mv[c];
+        const int pos0 = (e >= 0) ? cnt[warp * E + e] : 0;
+        __syncwarp();
+        if (e >= 0) {
+          const int pos = pos0 + __popc(m & lt_mask);
+          if constexpr (STAGED) out[pos] = static_cast<uint16_t>(a);
+          else sorted_ids[pos] = a;
+          if (lane == __ffs(m) - 1) cnt[warp * E + e] = pos0 + __popc(m);
+        }
+        __syncwarp();
+      }
+    }
   }
 
-  // padding rows of every expert and the block table
-  for (int e = tid; e < E; e += kAlignThreads) {
-    const int s = start[e], c = tot[e], p = (c + BM - 1) / BM * BM;
-    for (int pos = s + c; pos < s + p; ++pos) sorted_ids[pos] = n;
-    for (int b = s / BM; b < (s + p) / BM; ++b) block_expert[b] = e;
+  if constexpr (STAGED) {
+    __syncthreads();
+    // coalesced write-out: every padded position looks up its block's expert
+    const long long nb_used = total / BM;
+    for (long long p = tid; p < cap; p += kAlignThreads) {
+      int v = n;
+      if (p < total) {
+        const int e = blk[p / BM];
+        const int r = static_cast<int>(p) - start[e];
+        if (r < tot[e]) v = out[cstart[e] + r];
+      }
+      sorted_ids[p] = v;
+    }
+    for (long long b = tid; b < nblocks_cap; b += kAlignThreads)
+      block_expert[b] = (b < nb_used) ? blk[b] : -1;
+  } else {
+    // padding rows of every expert and the block table
+    for (int e = tid; e < E; e += kAlignThreads) {
+      const int s = start[e], c = tot[e], p = (c + BM - 1) / BM * BM;
+      for (int pos = s + c; pos < s + p; ++pos) sorted_ids[pos] = n;
+      for (int b = s / BM; b < (s + p) / BM; ++b) block_expert[b] = e;
+    }
+    // tail up to the capacity
+    for (long long pos = total + tid; pos < cap; pos += kAlignThreads) sorted_ids[pos] = n;
+    for (long long b = total / BM + tid; b < nblocks_cap; b += kAlignThreads) block_expert[b] = -1;
   }
-  // tail up to the capacity
-  for (long long pos = total + tid; pos < cap; pos += kAlignThreads) sorted_ids[pos] = n;
-  for (long long b = total / BM + tid; b < nblocks_cap; b += kAlignThreads) block_expert[b] = -1;
   if (tid == 0) *npp = total;
 }
 
@@ -131,17 +257,26 @@ int launch_align(const int32_t* topk_ids, int T, int k, int E, int block_m, int3
                  int64_t cap_rows, int32_t* block_expert, int32_t* num_post_padded, int* err,
                  cudaStream_t stream) {
   const int n = T * k;
-  const size_t smem = (32 * static_cast<size_t>(E) + 2 * E + 32) * sizeof(int);
+  const long long nbc = (cap_rows + block_m - 1) / block_m;
+  const AlignSmem staged = align_smem(n, E, nbc);
+  const size_t plain = (32 * static_cast<size_t>(E) + 3 * static_cast<size_t>(E) + 32) * 4;
+  constexpr size_t kMaxSmem = 227 * 1024;
   static bool attr_set = false;
   if (!attr_set) {
-    if (cudaFuncSetAttribute(align_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             32 * 1024 * 4 + 2 * 1024 * 4 + 128) != cudaSuccess)
+    if (cudaFuncSetAttribute(align_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kMaxSmem)) != cudaSuccess ||
+        cudaFuncSetAttribute(align_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kMaxSmem)) != cudaSuccess)
       return -1;
     attr_set = true;
   }
-  const long long nbc = (cap_rows + block_m - 1) / block_m;
-  align_kernel<<<1, kAlignThreads, smem, stream>>>(topk_ids, n, E, block_m, sorted_ids, cap_rows,
-                                                    block_expert, nbc, num_post_padded, err);
+  // 16-bit staging holds assignment ids below 65,535 and expert ids below 65,535
+  if (staged.bytes <= kMaxSmem && n < 65535)
+    align_kernel<true><<<1, kAlignThreads, staged.bytes, stream>>>(
+        topk_ids, n, E, block_m, sorted_ids, cap_rows, block_expert, nbc, num_post_padded, err);
+  else
+    align_kernel<false><<<1, kAlignThreads, plain, stream>>>(
+        topk_ids, n, E, block_m, sorted_ids, cap_rows, block_expert, nbc, num_post_padded, err);
   return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 

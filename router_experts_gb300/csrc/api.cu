@@ -264,8 +264,9 @@ static int expert_gemm(int kind, const void* act, int act_dt, const void* w, int
   if (!act || !w || !sorted_ids || !block_expert || !npp || !ws) return MOE_ERR_ARG;
   if (kind == 0 && !inter) return MOE_ERR_ARG;
   if (kind == 1 && (!topk_weights || !stage)) return MOE_ERR_ARG;
-  if (!aligned(ws, 256) || !aligned(act, 16) || !aligned(w, 16) || (inter && !aligned(inter, 16)) ||
-      (stage && !aligned(stage, 16)))
+  // the intermediate and the stage are written with 32-byte stores
+  if (!aligned(ws, 256) || !aligned(act, 16) || !aligned(w, 16) || (inter && !aligned(inter, 32)) ||
+      (stage && !aligned(stage, 32)))
     return MOE_ERR_ARG;
   const FfnLayout L = ffn_layout(T, F, E, k, block_m, inter_in_ws);
   if (ws_bytes < kWsHeaderBytes + L.total) return MOE_ERR_ARG;

@@ -41,32 +41,39 @@ constexpr int kThreads = 256;
 constexpr int kBK = 64;                 // K elements per stage (128 bytes of bf16)
 constexpr int kStageBudget = 220 * 1024;
 
+// Tile geometry.
+//   Swap tiles (BLOCK_M 16 / 64): A = 128 weight rows (GEMM1: 128 gate rows
+//   and the matching 128 up rows, two MMAs per K step), B = the block's BM
+//   token rows; double-buffered TMEM accumulators; optional split-K.
+//   Row tiles (BLOCK_M 128): A = the block's 128 token rows, B = 256 weight
+//   rows (GEMM1: 128 gate rows + the matching 128 up rows, two TMA boxes, so
+//   the epilogue pairs column c with column c + 128); one 128x256 MMA per K
+//   step; two 256-column accumulators, double-buffered.
 template <int KIND, int BM>
 struct Cfg {
   static constexpr bool SWAP = BM < 128;
   static constexpr bool GATHER = KIND == 0;
   static constexpr int NT = (KIND == 0) ? 128 : (SWAP ? 128 : 256);  // output tile width
-  static constexpr int A_BYTES = (KIND == 0 && SWAP) ? 2 * 128 * 128 : 128 * 128;
-  static constexpr int B_ROWS = SWAP ? BM : 256;
-  static constexpr int B_BYTES = B_ROWS * 128;
+  static constexpr int A_BYTES = (SWAP && KIND == 0) ? 2 * 128 * 128 : 128 * 128;
+  static constexpr int B_BYTES = SWAP ? BM * 128 : 256 * 128;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int STAGES_RAW = kStageBudget / STAGE_BYTES;
   static constexpr int STAGES = STAGES_RAW > 12 ? 12 : STAGES_RAW;
-  static constexpr int ACC_COLS = (KIND == 0 && SWAP) ? 2 * BM : (SWAP ? BM : 256);
-  static constexpr int TMEM_COLS = (2 * ACC_COLS <= 32)    ? 32
+  static constexpr int ACC_COLS = SWAP ? ((KIND == 0) ? 2 * BM : BM) : 256;
+  static constexpr int TMEM_COLS = !SWAP                   ? 512
+                                   : (2 * ACC_COLS <= 32)  ? 32
                                    : (2 * ACC_COLS <= 64)  ? 64
                                    : (2 * ACC_COLS <= 128) ? 128
                                    : (2 * ACC_COLS <= 256) ? 256
                                                            : 512;
-  // bytes delivered by TMA per stage
-  static constexpr int TX_BYTES = GATHER ? (SWAP ? A_BYTES : B_BYTES) : STAGE_BYTES;
   static constexpr uint32_t IDESC = SWAP ? idesc_bf16_f32(128, BM) : idesc_bf16_f32(128, 256);
-  // gather: rows of the token tile, 16-byte chunks per thread per stage
+  // gather: 16-byte chunks per gather thread per stage (64 threads, 8 chunks
+  // per 128-byte token row)
   static constexpr int G_ROWS = SWAP ? BM : 128;
-  static constexpr int G_PER_THREAD = G_ROWS / 8;  // 64 threads, 8 chunks per row
-  static constexpr int G_LAG = (STAGES - 1) < 3 ? (STAGES - 1) : 3;
-  static constexpr int BAR_BYTES = 256;
+  static constexpr int G_PER_THREAD = G_ROWS / 8;
+  static constexpr int BAR_BYTES = 512;
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + BAR_BYTES;
+  static_assert(G_PER_THREAD >= 2 && G_ROWS % 8 == 0, "gather split");
   static_assert(STAGE_BYTES % 1024 == 0, "stage tiles must keep 1024-byte alignment");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
@@ -93,6 +100,9 @@ struct Sched {
   int nblk, ntiles, KB, S, num_units;
 };
 
+// Work decomposition, identical in every CTA: unit = (block, output tile,
+// K split); blocks major, so the units of one block (and the blocks of one
+// expert) run side by side and share their operand tiles through L2.
 template <int KIND, int BM>
 MOE_DEV Sched make_sched(const FfnParams& p) {
   using C = Cfg<KIND, BM>;
@@ -135,6 +145,7 @@ MOE_DEV void load_cols(uint32_t taddr, float (&v)[16]) {
   uint32_t r[16];
   tmem_ld16(taddr, r);
   tmem_ld_wait();
+  reg_fence16(r);
 #pragma unroll
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
@@ -162,8 +173,9 @@ MOE_DEV void load_partial_cols(const float* base, size_t slot_stride, int S, flo
   }
 }
 
-// Epilogue of one output tile for the thread owning accumulator row `row`.
-// `fetch(col, v)` returns 16 accumulator columns starting at `col`.
+// Epilogue of one swap tile (BLOCK_M 16/64) for the thread owning TMEM lane
+// `row` (a feature of GEMM1, an output column of GEMM2).  `fetch(col, v)`
+// returns 16 accumulator columns (tokens of the block) starting at `col`.
 template <int KIND, int BM, class Fetch>
 MOE_DEV void epilogue_tile(const FfnParams& p, const Unit& u, int row, Fetch&& fetch) {
   using C = Cfg<KIND, BM>;
@@ -181,31 +193,11 @@ MOE_DEV void epilogue_tile(const FfnParams& p, const Unit& u, int row, Fetch&& f
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
           const size_t prow = static_cast<size_t>(u.b) * BM + c0 + c;
-          inter[prow * p.F + f] = __float2bfloat16_rn(silu_f(g[c]) * v[c]);
+          inter[prow * p.F + f] = __float2bfloat16_rn(swiglu_f(g[c], v[c]));
         }
       }
     }
-  } else if constexpr (KIND == 0) {
-    // row = token row of the block; columns: gate features [0,128), up [128,256)
-    const size_t prow = static_cast<size_t>(u.b) * BM + row;
-    __nv_bfloat16* inter = reinterpret_cast<__nv_bfloat16*>(p.inter);
-#pragma unroll 1
-    for (int c0 = 0; c0 < 128; c0 += 16) {
-      float g[16], v[16];
-      fetch(c0, g);
-      fetch(128 + c0, v);
-      const int f = u.n * C::NT + c0;
-      if (f + 16 <= p.F) {
-        uint32_t w[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-          w[i] = pack_bf16x2(silu_f(g[2 * i]) * v[2 * i], silu_f(g[2 * i + 1]) * v[2 * i + 1]);
-        uint4* dst = reinterpret_cast<uint4*>(inter + prow * p.F + f);
-        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-      }
-    }
-  } else if constexpr (C::SWAP) {
+  } else {
     // row = output column h of the layer; columns: the block's tokens
     const int h = u.n * C::NT + row;
     __nv_bfloat16* stage = reinterpret_cast<__nv_bfloat16*>(p.stage);
@@ -222,25 +214,59 @@ MOE_DEV void epilogue_tile(const FfnParams& p, const Unit& u, int row, Fetch&& f
         }
       }
     }
-  } else {
-    // row = token row of the block; columns: output columns h
-    const int a = __ldg(p.sorted_ids + static_cast<size_t>(u.b) * BM + row);
-    const bool valid = a >= 0 && a < nk;
-    const float w = valid ? __ldg(p.topk_weights + a) : 0.f;
-    __nv_bfloat16* stage = reinterpret_cast<__nv_bfloat16*>(p.stage);
-#pragma unroll 1
-    for (int c0 = 0; c0 < 256; c0 += 16) {
-      float v[16];
-      fetch(c0, v);
-      const int h = u.n * C::NT + c0;
-      if (valid && h + 16 <= p.H) {
-        uint32_t o[8];
+  }
+}
+
+// Epilogue of a 128-token tile (BLOCK_M 128) straight from TMEM, with the
+// TMEM load of chunk c+1 in flight while chunk c is computed and stored.
+template <int KIND>
+MOE_DEV void epilogue_rows128(const FfnParams& p, const Unit& u, int row, uint32_t tb) {
+  constexpr int NCH = (KIND == 0) ? 8 : 16;  // 16-column chunks of the tile
+  constexpr int NT = (KIND == 0) ? 128 : 256;
+  const size_t prow = static_cast<size_t>(u.b) * 128 + row;
+  int a = 0;
+  bool valid = true;
+  float w = 1.f;
+  if constexpr (KIND == 1) {
+    a = __ldg(p.sorted_ids + prow);
+    valid = a >= 0 && a < p.T * p.k;
+    w = valid ? __ldg(p.topk_weights + a) : 0.f;
+  }
+  uint32_t ra[2][16], rb[2][16];
+  tmem_ld16(tb, ra[0]);
+  if constexpr (KIND == 0) tmem_ld16(tb + 128, rb[0]);
+  tmem_ld_wait();
+  reg_fence16(ra[0]);
+  if constexpr (KIND == 0) reg_fence16(rb[0]);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) o[i] = pack_bf16x2(v[2 * i] * w, v[2 * i + 1] * w);
-        uint4* dst = reinterpret_cast<uint4*>(stage + static_cast<size_t>(a) * p.H + h);
-        dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
-        dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
-      }
+  for (int c = 0; c < NCH; ++c) {
+    const int cur = c & 1, nxt = cur ^ 1;
+    if (c + 1 < NCH) {
+      tmem_ld16(tb + 16 * (c + 1), ra[nxt]);
+      if constexpr (KIND == 0) tmem_ld16(tb + 128 + 16 * (c + 1), rb[nxt]);
+    }
+    const int col = u.n * NT + 16 * c;
+    uint32_t o[8];
+    if constexpr (KIND == 0) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        o[i] = pack_bf16x2(swiglu_f(__uint_as_float(ra[cur][2 * i]), __uint_as_float(rb[cur][2 * i])),
+                           swiglu_f(__uint_as_float(ra[cur][2 * i + 1]),
+                                    __uint_as_float(rb[cur][2 * i + 1])));
+      if (col + 16 <= p.F)
+        st_global_v8(reinterpret_cast<__nv_bfloat16*>(p.inter) + prow * p.F + col, o);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        o[i] = pack_bf16x2(__uint_as_float(ra[cur][2 * i]) * w,
+                           __uint_as_float(ra[cur][2 * i + 1]) * w);
+      if (valid && col + 16 <= p.H)
+        st_global_v8(reinterpret_cast<__nv_bfloat16*>(p.stage) + static_cast<size_t>(a) * p.H + col, o);
+    }
+    if (c + 1 < NCH) {
+      tmem_ld_wait();
+      reg_fence16(ra[nxt]);
+      if constexpr (KIND == 0) reg_fence16(rb[nxt]);
     }
   }
 }
@@ -292,7 +318,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool alive = true;
       for (int uu = blockIdx.x; alive && uu < sc.num_units; uu += gridDim.x) {
         const Unit u = decode_unit<KIND, BM>(p, sc, uu);
+        // row tiles: the CTA's next unit, so the L2 warm-up of weight tiles
+        // runs across the unit boundary (decode tiles stream each weight once
+        // and gain nothing from it)
+        const bool has_next = uu + static_cast<int>(gridDim.x) < sc.num_units;
+        const Unit nu =
+            has_next ? decode_unit<KIND, BM>(p, sc, uu + gridDim.x) : u;
         for (int kb = u.kb0; kb < u.kb1; ++kb, ++it) {
+          if constexpr (!C::SWAP) {
+            int tkb = kb + C::STAGES;
+            const Unit* tu = &u;
+            if (tkb >= u.kb1 && has_next) {
+              tkb = nu.kb0 + (tkb - u.kb1);
+              tu = &nu;
+            }
+            if (tkb < tu->kb1) {
+              if constexpr (KIND == 0) {
+                const int grow = tu->e * 2 * p.F + tu->n * C::NT;
+                tma_prefetch_l2_2d(&tm_w, tkb * kBK, grow);
+                tma_prefetch_l2_2d(&tm_w, tkb * kBK, grow + p.F);
+              } else {
+                tma_prefetch_l2_2d(&tm_w, tkb * kBK, tu->e * p.H + tu->n * C::NT);
+              }
+            }
+          }
           const int st = it % C::STAGES;
           const uint32_t ph = (it / C::STAGES) & 1u;
           if (!mbar_wait(&empty_bar[st], ph ^ 1u, abort_flag, p.err)) {
@@ -301,20 +350,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           uint8_t* sa = smem + st * C::STAGE_BYTES;
           uint8_t* sb = sa + C::A_BYTES;
-          mbar_arrive_expect_tx(&full_bar[st], C::TX_BYTES);
           const int kc = kb * kBK;
           if constexpr (KIND == 0) {
             const int grow = u.e * 2 * p.F + u.n * C::NT;
-            const int urow = grow + p.F;
             uint8_t* dst = C::SWAP ? sa : sb;
+            mbar_arrive_expect_tx(&full_bar[st], 2 * 128 * 128);
             tma_load_2d(dst, &tm_w, &full_bar[st], kc, grow);
-            tma_load_2d(dst + 128 * 128, &tm_w, &full_bar[st], kc, urow);
+            tma_load_2d(dst + 128 * 128, &tm_w, &full_bar[st], kc, grow + p.F);
           } else {
             const int wrow = u.e * p.H + u.n * C::NT;
             if constexpr (C::SWAP) {
+              mbar_arrive_expect_tx(&full_bar[st], C::STAGE_BYTES);
               tma_load_2d(sa, &tm_w, &full_bar[st], kc, wrow);
               tma_load_2d(sb, &tm_in, &full_bar[st], kc, u.b * BM);
             } else {
+              mbar_arrive_expect_tx(&full_bar[st], C::STAGE_BYTES);
               tma_load_2d(sa, &tm_in, &full_bar[st], kc, u.b * BM);
               tma_load_2d(sb, &tm_w, &full_bar[st], kc, wrow);
             }
@@ -341,6 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             alive = false;
             break;
           }
+          if constexpr (C::GATHER) fence_proxy_async_smem();  // cp.async rows -> tensor core
           tc_fence_after();
           const uint32_t a_addr = smem_u32(smem + st * C::STAGE_BYTES);
           const uint32_t b_addr = a_addr + C::A_BYTES;
@@ -348,12 +399,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kk = 0; kk < kBK / 16; ++kk) {
             const uint32_t acc = (kb > u.kb0 || kk > 0) ? 1u : 0u;
             const uint64_t bdesc = sw128_desc(b_addr + kk * 32);
-            if constexpr (KIND == 0 && C::SWAP) {
-              umma_f16(d, sw128_desc(a_addr + kk * 32), bdesc, C::IDESC, acc);
+            umma_f16(d, sw128_desc(a_addr + kk * 32), bdesc, C::IDESC, acc);
+            if constexpr (KIND == 0 && C::SWAP)
               umma_f16(d + BM, sw128_desc(a_addr + 128 * 128 + kk * 32), bdesc, C::IDESC, acc);
-            } else {
-              umma_f16(d, sw128_desc(a_addr + kk * 32), bdesc, C::IDESC, acc);
-            }
           }
           umma_commit(&empty_bar[st]);
         }
@@ -369,7 +417,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const __nv_bfloat16* x = reinterpret_cast<const __nv_bfloat16*>(p.x);
       const int nk = p.T * p.k;
       uint32_t it = 0;
-      int pending = 0;
       bool alive = true;
       for (int uu = blockIdx.x; alive && uu < sc.num_units; uu += gridDim.x) {
         const Unit u = decode_unit<KIND, BM>(p, sc, uu);
@@ -397,21 +444,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t dst = tile + r * 128 + ((chunk ^ (r & 7)) << 4);
             cp_async_16(dst, nbytes[i] ? src[i] + kb * kBK : src[i], nbytes[i]);
           }
-          cp_async_commit();
-          ++pending;
-          if (pending > C::G_LAG) {
-            cp_async_wait<C::G_LAG>();
-            fence_proxy_async_smem();
-            mbar_arrive(&full_bar[(it - C::G_LAG) % C::STAGES]);
-            --pending;
-          }
+          // the stage barrier counts this thread's arrival when its copies land;
+          // the MMA issuer orders them before its tensor-core reads (proxy fence)
+          cp_async_mbar_arrive_noinc(&full_bar[st]);
         }
       }
-      cp_async_wait<0>();
-      fence_proxy_async_smem();
-      if (alive) {
-        for (int j = pending; j > 0; --j) mbar_arrive(&full_bar[(it - j) % C::STAGES]);
-      }
+      cp_async_wait_all();
     }
   } else {
     // ---------------- epilogue ----------------
@@ -427,10 +465,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool ok = mbar_wait(&tfull_bar[buf], aph, abort_flag, p.err);
       if (named_bar_any(1, 128, !ok || *abort_flag)) break;
       tc_fence_after();
-      const uint32_t tb = tmem_base + (static_cast<uint32_t>(ew * 32) << 16) + buf * C::ACC_COLS;
+      const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(ew * 32) << 16);
+      const uint32_t tb = lane_base + buf * C::ACC_COLS;
       if (sc.S == 1) {
-        epilogue_tile<KIND, BM>(p, u, row,
-                                [&](int col, float (&v)[16]) { load_cols(tb + col, v); });
+        if constexpr (!C::SWAP)
+          epilogue_rows128<KIND>(p, u, row, tb);
+        else
+          epilogue_tile<KIND, BM>(p, u, row,
+                                  [&](int col, float (&v)[16]) { load_cols(tb + col, v); });
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty_bar[buf]);
@@ -450,17 +492,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty_bar[buf]);
-        __threadfence();
+        // one thread draws the ticket: release of the 128 rows just written,
+        // acquire of the other splits' rows
         named_bar_sync(1, 128);
         if (et == 0) {
-          const int old = atomicAdd(p.tickets + u.ug, 1);
+          const int old = ticket_add_acq_rel(p.tickets + u.ug, 1);
           const int last = (old == sc.S - 1);
-          if (last) p.tickets[u.ug] = 0;  // ready for the next launch
+          if (last) store_relaxed_gpu(p.tickets + u.ug, 0);  // ready for the next launch
           *last_flag = last;
         }
         named_bar_sync(1, 128);
         if (*last_flag) {
-          __threadfence();
           const float* base0 = p.partial + static_cast<size_t>(u.ug) * sc.S * slot_stride +
                                static_cast<size_t>(row) * C::ACC_COLS;
           epilogue_tile<KIND, BM>(p, u, row, [&](int col, float (&v)[16]) {

@@ -32,7 +32,6 @@ namespace {
 
 constexpr int kRouterThreads = 256;
 constexpr int kMaxSlotsPerLane = 16;  // E <= 512
-constexpr int kMaxK = 16;
 constexpr int kTargetCtas = 304;      // two CTAs per SM of a 152-SM part
 
 struct RouterArgs {
@@ -125,163 +124,150 @@ MOE_DEV void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-MOE_DEV bool beats(float ka, int ia, float kb, int ib) { return ka > kb || (ka == kb && ia < ib); }
-
-MOE_DEV float warp_max(float v) {
-#pragma unroll
-  for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  return v;
-}
 MOE_DEV float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   return v;
 }
 
-// Selection for one token by one warp.  `logit(i)` is the lane's i-th logit
-// (expert lane + 32 i).  Writes k ids and weights.
-MOE_DEV void select_token(const RouterArgs& a, int t, const float (&lg)[kMaxSlotsPerLane]) {
+// Selection for one token by one warp; E <= 32 * S (S slots per lane, expert
+// lane + 32 i in slot i).  `row` holds the token's E fp32 logits (shared
+// memory).  Every warp-wide argmax is two redux operations: the largest
+// order-mapped key, then the lowest expert id holding it.
+template <int S>
+MOE_DEV void select_token(const RouterArgs& a, int t, const float* row, const float* sbias) {
   const int lane = threadIdx.x & 31;
   const int E = a.E;
-  float sc[kMaxSlotsPerLane], key[kMaxSlotsPerLane];
-  bool ok[kMaxSlotsPerLane];
-  // scores
+  float sc[S], key[S];
+  bool ok[S];
+#pragma unroll
+  for (int i = 0; i < S; ++i) {
+    const int e = lane + 32 * i;
+    ok[i] = e < E;
+    sc[i] = ok[i] ? row[e] : -INFINITY;  // logits for now
+  }
   if (a.scoring == 0) {
     float m = -INFINITY;
 #pragma unroll
-    for (int i = 0; i < kMaxSlotsPerLane; ++i)
-      if (lane + 32 * i < E) m = fmaxf(m, lg[i]);
-    m = warp_max(m);
-    float s = 0.f;
+    for (int i = 0; i < S; ++i) m = fmaxf(m, sc[i]);
+    m = ord2f(__reduce_max_sync(0xffffffffu, f2ord(m)));
+    float sum = 0.f;
 #pragma unroll
-    for (int i = 0; i < kMaxSlotsPerLane; ++i) {
-      sc[i] = (lane + 32 * i < E) ? expf(lg[i] - m) : 0.f;
-      s += sc[i];
+    for (int i = 0; i < S; ++i) {
+      sc[i] = ok[i] ? expf(sc[i] - m) : 0.f;
+      sum += sc[i];
     }
-    s = warp_sum(s);
-    const float inv = 1.0f / s;
+    sum = warp_sum(sum);
+    const float inv = 1.0f / sum;
 #pragma unroll
-    for (int i = 0; i < kMaxSlotsPerLane; ++i) sc[i] *= inv;
+    for (int i = 0; i < S; ++i) sc[i] *= inv;
   } else {
 #pragma unroll
-    for (int i = 0; i < kMaxSlotsPerLane; ++i) sc[i] = 1.0f / (1.0f + expf(-lg[i]));
+    for (int i = 0; i < S; ++i) sc[i] = ok[i] ? 1.0f / (1.0f + expf(-sc[i])) : 0.f;
   }
 #pragma unroll
-  for (int i = 0; i < kMaxSlotsPerLane; ++i) {
+  for (int i = 0; i < S; ++i) {
     const int e = lane + 32 * i;
-    ok[i] = e < E;
-    key[i] = ok[i] ? sc[i] + (a.bias ? __ldg(a.bias + e) : 0.f) : -INFINITY;
+    key[i] = ok[i] ? sc[i] + sbias[e] : -INFINITY;
   }
-  // group-limited selection: keep the topk_group groups with the largest
-  // sum of their two best rank keys (lowest group id on ties)
+  // group-limited selection: keep the topk_group groups with the largest sum
+  // of their two best rank keys (lowest group id on ties)
   if (a.n_group > 1) {
     const int gs = E / a.n_group;
-    float my_g = -INFINITY;  // lane g holds the score of group g
-    for (int g = 0; g < a.n_group; ++g) {
-      float b1 = -INFINITY, b2 = -INFINITY;
+    int grp[S];
 #pragma unroll
-      for (int i = 0; i < kMaxSlotsPerLane; ++i) {
-        const int e = lane + 32 * i;
-        if (e < E && e / gs == g) {
+    for (int i = 0; i < S; ++i) grp[i] = ok[i] ? (lane + 32 * i) / gs : -1;
+    uint32_t my_g = 0;  // lane g: order-mapped score of group g
+    for (int g = 0; g < a.n_group; ++g) {
+      float t1 = -INFINITY, t2 = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < S; ++i) {
+        if (grp[i] == g) {
           const float v = key[i];
-          if (v > b1) {
-            b2 = b1;
-            b1 = v;
-          } else if (v > b2) {
-            b2 = v;
+          if (v > t1) {
+            t2 = t1;
+            t1 = v;
+          } else if (v > t2) {
+            t2 = v;
           }
         }
       }
-#pragma unroll
-      for (int o = 16; o; o >>= 1) {
-        const float o1 = __shfl_xor_sync(0xffffffffu, b1, o);
-        const float o2 = __shfl_xor_sync(0xffffffffu, b2, o);
-        const float n1 = fmaxf(b1, o1);
-        const float n2 = fmaxf(fminf(b1, o1), fmaxf(b2, o2));
-        b1 = n1;
-        b2 = n2;
-      }
-      if (lane == g) my_g = b1 + b2;
+      const uint32_t o1 = f2ord(t1);
+      const uint32_t b1 = __reduce_max_sync(0xffffffffu, o1);
+      const unsigned holders = __ballot_sync(0xffffffffu, o1 == b1);
+      uint32_t b2 = b1;
+      if (__popc(holders) < 2) b2 = __reduce_max_sync(0xffffffffu, o1 == b1 ? f2ord(t2) : o1);
+      if (lane == g) my_g = f2ord(ord2f(b1) + ord2f(b2));
     }
     uint32_t kept = 0;
     for (int r = 0; r < a.topk_group; ++r) {
-      float bv = (lane < a.n_group && !((kept >> lane) & 1u)) ? my_g : -INFINITY;
-      int bi = (lane < a.n_group && !((kept >> lane) & 1u)) ? lane : INT_MAX;
-#pragma unroll
-      for (int o = 16; o; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-        if (beats(ov, oi, bv, bi)) {
-          bv = ov;
-          bi = oi;
-        }
-      }
-      if (bi >= 0 && bi < 32) kept |= 1u << bi;
+      const bool cand = lane < a.n_group && !((kept >> lane) & 1u);
+      const uint32_t gmax = __reduce_max_sync(0xffffffffu, cand ? my_g : 0u);
+      const int sel = __reduce_min_sync(0xffffffffu, (cand && my_g == gmax) ? lane : 32);
+      if (sel < 32) kept |= 1u << sel;
     }
 #pragma unroll
-    for (int i = 0; i < kMaxSlotsPerLane; ++i) {
-      const int e = lane + 32 * i;
-      if (e < E && !((kept >> (e / gs)) & 1u)) ok[i] = false;
+    for (int i = 0; i < S; ++i)
+      if (ok[i] && !((kept >> grp[i]) & 1u)) ok[i] = false;
+  }
+  // k rounds of a warp argmax (largest key, lowest id on ties); lane j keeps
+  // the j-th winner
+  int my_id = -1;
+  float my_s = 0.f;
+  for (int j = 0; j < a.k; ++j) {
+    uint32_t bk = 0;
+    int be = INT_MAX;
+    float bs = 0.f;
+#pragma unroll
+    for (int i = 0; i < S; ++i) {
+      const uint32_t o = f2ord(key[i]);
+      if (ok[i] && (o > bk || (o == bk && lane + 32 * i < be))) {
+        bk = o;
+        be = lane + 32 * i;
+        bs = sc[i];
+      }
+    }
+    const uint32_t kmax = __reduce_max_sync(0xffffffffu, bk);
+    const int win = __reduce_min_sync(0xffffffffu, (be != INT_MAX && bk == kmax) ? be : INT_MAX);
+    const int owner = (win == INT_MAX) ? 0 : (win & 31);
+    const float ws = __shfl_sync(0xffffffffu, bs, owner);
+    if (lane == owner && win != INT_MAX) {
+#pragma unroll
+      for (int i = 0; i < S; ++i)
+        if (lane + 32 * i == win) ok[i] = false;
+    }
+    if (lane == j) {
+      my_id = (win == INT_MAX) ? -1 : win;
+      my_s = ws;
     }
   }
-  // k rounds of a warp argmax (largest key, lowest id on ties)
-  int win_e[kMaxK];
-  float win_s[kMaxK];
-#pragma unroll
-  for (int j = 0; j < kMaxK; ++j) {
-    win_e[j] = -1;
-    win_s[j] = 0.f;
-    if (j < a.k) {
-      float bk = -INFINITY, bs = 0.f;
-      int be = INT_MAX;
-#pragma unroll
-      for (int i = 0; i < kMaxSlotsPerLane; ++i) {
-        const int e = lane + 32 * i;
-        if (ok[i] && beats(key[i], e, bk, be)) {
-          bk = key[i];
-          be = e;
-          bs = sc[i];
-        }
-      }
-#pragma unroll
-      for (int o = 16; o; o >>= 1) {
-        const float ok2 = __shfl_xor_sync(0xffffffffu, bk, o);
-        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-        const float os = __shfl_xor_sync(0xffffffffu, bs, o);
-        if (beats(ok2, oe, bk, be)) {
-          bk = ok2;
-          be = oe;
-          bs = os;
-        }
-      }
-      win_e[j] = (be == INT_MAX) ? -1 : be;
-      win_s[j] = bs;
-#pragma unroll
-      for (int i = 0; i < kMaxSlotsPerLane; ++i)
-        if (lane + 32 * i == be) ok[i] = false;
-    }
+  const float sum = warp_sum(lane < a.k ? my_s : 0.f);
+  const float denom = a.renorm ? (sum + 1e-20f) : 1.0f;
+  if (lane < a.k) {
+    a.ids[static_cast<size_t>(t) * a.k + lane] = my_id;
+    a.wts[static_cast<size_t>(t) * a.k + lane] = my_s / denom * a.scaling;
   }
-  if (lane == 0) {
-    float sum = 0.f;
-#pragma unroll
-    for (int j = 0; j < kMaxK; ++j)
-      if (j < a.k) sum += win_s[j];
-    const float denom = a.renorm ? (sum + 1e-20f) : 1.0f;
-#pragma unroll
-    for (int j = 0; j < kMaxK; ++j) {
-      if (j < a.k) {
-        a.ids[static_cast<size_t>(t) * a.k + j] = win_e[j];
-        a.wts[static_cast<size_t>(t) * a.k + j] = win_s[j] / denom * a.scaling;
-      }
-    }
-  }
+}
+
+MOE_DEV void select_dispatch(const RouterArgs& a, int t, const float* row, const float* sbias) {
+  const int s = (a.E + 31) / 32;
+  if (s <= 1) select_token<1>(a, t, row, sbias);
+  else if (s <= 2) select_token<2>(a, t, row, sbias);
+  else if (s <= 4) select_token<4>(a, t, row, sbias);
+  else if (s <= 8) select_token<8>(a, t, row, sbias);
+  else if (s <= 9) select_token<9>(a, t, row, sbias);
+  else select_token<16>(a, t, row, sbias);
 }
 
 template <int XDT, int GDT, int NB8>
 __global__ void __launch_bounds__(kRouterThreads) router_kernel(const RouterArgs a) {
   constexpr int ET = 8 * NB8;
   constexpr int XP = SrcPieces<XDT>::P, GP = SrcPieces<GDT>::P;
-  __shared__ float red[8][16][ET];
+  // per-warp partial logits, later reused for the token tile's full logits
+  constexpr int kRedFloats = 8 * 16 * ET;
+  constexpr int kTileFloats = (16 + 1) * 32 * kMaxSlotsPerLane;  // 16 logit rows + bias
+  __shared__ __align__(16) float sbuf[kRedFloats > kTileFloats ? kRedFloats : kTileFloats];
+  float(*red)[16][ET] = reinterpret_cast<float(*)[16][ET]>(sbuf);
   __shared__ int s_last;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -336,36 +322,62 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(const RouterArgs
     const int t = t0 + r, e = e0 + c;
     if (t < a.T && e < a.E) a.scratch[(static_cast<size_t>(ks) * a.T + t) * a.E + e] = v;
   }
-  // last CTA of this token tile does the selection
-  __threadfence();
+  // last CTA of this token tile does the selection: one thread draws a
+  // ticket (release of this CTA's partials, acquire of the others')
   __syncthreads();
   if (threadIdx.x == 0) {
     const int total = gridDim.x * gridDim.z;
-    const int old = atomicAdd(a.tickets + blockIdx.y, 1);
+    const int old = ticket_add_acq_rel(a.tickets + blockIdx.y, 1);
     const int last = (old == total - 1);
-    if (last) a.tickets[blockIdx.y] = 0;  // ready for the next launch
+    if (last) store_relaxed_gpu(a.tickets + blockIdx.y, 0);  // ready for the next launch
     s_last = last;
   }
   __syncthreads();
   if (!s_last) return;
-  __threadfence();
-  for (int r = warp; r < 16; r += 8) {
-    const int t = t0 + r;
-    if (t >= a.T) break;
-    float lg[kMaxSlotsPerLane];
+  // sum the K-slice partials of the tile's logits in slice order.  Each thread
+  // owns up to kPer logits and issues all their loads (every slice) before
+  // summing, so the reduction costs one L2 round trip; the bias rides along.
+  const int rows = min(16, a.T - t0);
+  float* tile = sbuf;                                   // [16][E]
+  float* sbias = sbuf + 16 * 32 * kMaxSlotsPerLane;    // [E], after the 16 logit rows
+  const size_t slice = static_cast<size_t>(a.T) * a.E;
+  const int nlog = rows * a.E;
+  constexpr int kPer = 8;
+  for (int base = threadIdx.x; base < nlog; base += kRouterThreads * kPer) {
+    float acc[kPer];
 #pragma unroll
-    for (int i = 0; i < kMaxSlotsPerLane; ++i) {
-      const int e = lane + 32 * i;
-      float v = -INFINITY;
-      if (e < a.E) {
-        v = __ldcg(a.scratch + static_cast<size_t>(t) * a.E + e);
-        for (int s = 1; s < a.KS; ++s)
-          v += __ldcg(a.scratch + (static_cast<size_t>(s) * a.T + t) * a.E + e);
+    for (int u = 0; u < kPer; ++u) {
+      const int idx = base + u * kRouterThreads;
+      acc[u] = 0.f;
+      if (idx < nlog) {
+        const int r = idx / a.E, e = idx - r * a.E;
+        acc[u] = __ldcg(a.scratch + static_cast<size_t>(t0 + r) * a.E + e);
       }
-      lg[i] = v;
     }
-    select_token(a, t, lg);
+    for (int s = 1; s < a.KS; ++s) {
+      float part[kPer];
+#pragma unroll
+      for (int u = 0; u < kPer; ++u) {
+        const int idx = base + u * kRouterThreads;
+        part[u] = 0.f;
+        if (idx < nlog) {
+          const int r = idx / a.E, e = idx - r * a.E;
+          part[u] = __ldcg(a.scratch + s * slice + static_cast<size_t>(t0 + r) * a.E + e);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kPer; ++u) acc[u] += part[u];
+    }
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int idx = base + u * kRouterThreads;
+      if (idx < nlog) tile[idx] = acc[u];
+    }
   }
+  for (int e = threadIdx.x; e < a.E; e += kRouterThreads)
+    sbias[e] = a.bias ? __ldg(a.bias + e) : 0.f;
+  __syncthreads();
+  for (int r = warp; r < rows; r += 8) select_dispatch(a, t0 + r, tile + r * a.E, sbias);
 }
 
 template <int XDT, int GDT>
@@ -388,7 +400,8 @@ RouterPlan plan_router(int T, int H, int E) {
   p.nt = (T + 15) / 16;
   p.ks = 1;
   const int steps = H / 32;
-  while (p.ks < 16 && (long long)p.ne * p.nt * p.ks < kTargetCtas && steps % (2 * p.ks) == 0)
+  // grow the K split while the grid stays within one wave (two CTAs per SM)
+  while (p.ks < 16 && (long long)p.ne * p.nt * p.ks * 2 <= kTargetCtas && steps % (2 * p.ks) == 0)
     p.ks *= 2;
   p.scratch_bytes = align_up(static_cast<size_t>(p.ks) * T * E * sizeof(float), 256);
   return p;
