@@ -39,13 +39,20 @@ static bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_
 struct FfnLayout {
   size_t inter, partial, total;  // offsets from the region start
 };
-static FfnLayout ffn_layout(int T, int F, int E, int k, int block_m, bool with_inter) {
+// The intermediate: bf16 [cap, F]; low-bit: e4m3 codes [cap, F] then UE8M0
+// scales [cap, F/32].
+static size_t inter_bytes(size_t cap, int F, int act_dt) {
+  if (act_dt == MOE_DT_E4M3) return align_up(cap * F, 256) + align_up(cap * (F / 32), 256);
+  return align_up(cap * F * 2, 256);
+}
+static FfnLayout ffn_layout(int T, int F, int E, int k, int block_m, bool with_inter,
+                            int act_dt = MOE_DT_BF16) {
   FfnLayout L{};
   size_t off = 0;
   if (with_inter) {
     const size_t cap = static_cast<size_t>(T) * k + static_cast<size_t>(E) * (block_m - 1);
     L.inter = off;
-    off += align_up(cap * F * 2, 256);
+    off += inter_bytes(cap, F, act_dt);
   }
   L.partial = off;
   off += ffn_partial_bytes(block_m);
@@ -57,7 +64,8 @@ struct LayerLayout {
   size_t ids, wts, sorted, blk, npp, stage, router, ffn, total;
   int64_t cap;
 };
-static LayerLayout layer_layout(int T, int H, int F, int E, int k, int block_m) {
+static LayerLayout layer_layout(int T, int H, int F, int E, int k, int block_m,
+                                int act_dt = MOE_DT_BF16) {
   LayerLayout L{};
   size_t off = kWsHeaderBytes;
   const size_t nk = static_cast<size_t>(T) * k;
@@ -77,7 +85,7 @@ static LayerLayout layer_layout(int T, int H, int F, int E, int k, int block_m) 
   L.router = off;
   off += plan_router(T, H, E).scratch_bytes;
   L.ffn = off;
-  off += ffn_layout(T, F, E, k, block_m, true).total;
+  off += ffn_layout(T, F, E, k, block_m, true, act_dt).total;
   L.total = off;
   return L;
 }
@@ -124,7 +132,8 @@ static int check_ffn(int act_dt, int w_dt, int T, int H, int F, int E, int k, in
       static_cast<int64_t>(E) * H > 0x7fffffffll)
     return MOE_ERR_ARG;
   if (act_dt == MOE_DT_BF16 && w_dt == MOE_DT_BF16) return MOE_OK;
-  if (act_dt == MOE_DT_E4M3 && w_dt == MOE_DT_E2M1) return MOE_ERR_UNSUPPORTED;
+  if (act_dt == MOE_DT_E4M3 && w_dt == MOE_DT_E2M1)
+    return (F % 64 == 0) ? MOE_OK : MOE_ERR_ARG;  // both contractions in whole 64-steps
   return MOE_ERR_UNSUPPORTED;
 }
 
@@ -248,9 +257,49 @@ int moe_align(const int32_t* topk_ids, int T, int k, int E, int block_m, int32_t
 // ---- expert GEMMs --------------------------------------------------------------
 size_t moe_ffn_workspace_bytes(int T, int H, int F, int E, int k, int block_m, int act_dt) {
   (void)H;
-  (void)act_dt;
   if (T < 0 || F <= 0 || E <= 0 || k <= 0 || check_block_m(block_m) != MOE_OK) return 0;
-  return kWsHeaderBytes + ffn_layout(T, F, E, k, block_m, true).total;
+  return kWsHeaderBytes + ffn_layout(T, F, E, k, block_m, true, act_dt).total;
+}
+
+// Low-bit path: kind 0 reads x codes/scales and writes the e4m3 intermediate
+// (codes + scales); kind 1 reads it and writes the bf16 stage.
+static int expert_gemm_lowbit(int kind, const void* act, const uint8_t* act_scale,
+                              const void* w, const uint8_t* w_scale, int T, int H, int F, int E,
+                              int k, int block_m, const int32_t* sorted_ids,
+                              const int32_t* block_expert, const int32_t* npp, int64_t cap_rows,
+                              uint8_t* inter_q, uint8_t* inter_scale, const float* topk_weights,
+                              void* stage, void* ws, cudaStream_t stream) {
+  if (!act || !act_scale || !w || !w_scale || !sorted_ids || !block_expert || !npp || !ws)
+    return MOE_ERR_ARG;
+  if (kind == 0 && (!inter_q || !inter_scale)) return MOE_ERR_ARG;
+  if (kind == 1 && (!topk_weights || !stage)) return MOE_ERR_ARG;
+  if (!aligned(act, 16) || !aligned(w, 16) || !aligned(w_scale, 2) ||
+      (inter_q && !aligned(inter_q, 32)) || (stage && !aligned(stage, 32)))
+    return MOE_ERR_ARG;
+  LowbitParams p{};
+  p.sorted_ids = sorted_ids;
+  p.block_expert = block_expert;
+  p.num_post_padded = npp;
+  p.act = static_cast<const uint8_t*>(act);
+  p.act_scale = act_scale;
+  p.w = static_cast<const uint8_t*>(w);
+  p.w_scale = w_scale;
+  p.inter_q = inter_q;
+  p.inter_scale = inter_scale;
+  p.topk_weights = topk_weights;
+  p.stage = static_cast<__nv_bfloat16*>(stage);
+  p.err = err_word(ws);
+  p.T = T;
+  p.H = H;
+  p.F = F;
+  p.E = E;
+  p.k = k;
+  p.BM = block_m;
+  p.cap_rows = static_cast<int>(cap_rows);
+  const int sms = device_num_sms();
+  if (sms <= 0) return cuda_fail("cudaDeviceGetAttribute", cudaGetLastError());
+  if (launch_lowbit_gemm(kind, p, sms, stream) != 0) return launch_fail("low-bit GEMM kernel");
+  return MOE_OK;
 }
 
 static int expert_gemm(int kind, const void* act, int act_dt, const void* w, int w_dt, int T,
@@ -292,9 +341,16 @@ int moe_expert_gemm1(const void* x, int act_dt, const uint8_t* x_scale, const vo
                      int block_m, const int32_t* sorted_ids, const int32_t* block_expert,
                      const int32_t* num_post_padded, int64_t cap_rows, void* inter,
                      uint8_t* inter_scale, void* ws, size_t ws_bytes, void* stream) {
-  (void)x_scale;
-  (void)w13_scale;
-  (void)inter_scale;
+  if (act_dt == MOE_DT_E4M3) {
+    const int rc = check_ffn(act_dt, w_dt, T, H, F, E, k, block_m, cap_rows);
+    if (rc != MOE_OK) return rc;
+    if (T == 0) return MOE_OK;
+    if (ws_bytes < kWsHeaderBytes || !aligned(ws, 256)) return MOE_ERR_ARG;
+    return expert_gemm_lowbit(0, x, x_scale, w13, w13_scale, T, H, F, E, k, block_m, sorted_ids,
+                              block_expert, num_post_padded, cap_rows,
+                              static_cast<uint8_t*>(inter), inter_scale, nullptr, nullptr, ws,
+                              static_cast<cudaStream_t>(stream));
+  }
   return expert_gemm(0, x, act_dt, w13, w_dt, T, H, F, E, k, block_m, sorted_ids, block_expert,
                      num_post_padded, cap_rows, inter, nullptr, nullptr, ws, ws_bytes, false,
                      static_cast<cudaStream_t>(stream));
@@ -306,8 +362,15 @@ int moe_expert_gemm2(const void* inter, const uint8_t* inter_scale, int act_dt, 
                      const int32_t* num_post_padded, int64_t cap_rows,
                      const float* topk_weights, void* stage, void* ws, size_t ws_bytes,
                      void* stream) {
-  (void)inter_scale;
-  (void)w2_scale;
+  if (act_dt == MOE_DT_E4M3) {
+    const int rc = check_ffn(act_dt, w_dt, T, H, F, E, k, block_m, cap_rows);
+    if (rc != MOE_OK) return rc;
+    if (T == 0) return MOE_OK;
+    if (ws_bytes < kWsHeaderBytes || !aligned(ws, 256)) return MOE_ERR_ARG;
+    return expert_gemm_lowbit(1, inter, inter_scale, w2, w2_scale, T, H, F, E, k, block_m,
+                              sorted_ids, block_expert, num_post_padded, cap_rows, nullptr,
+                              nullptr, topk_weights, stage, ws, static_cast<cudaStream_t>(stream));
+  }
   return expert_gemm(1, inter, act_dt, w2, w_dt, T, H, F, E, k, block_m, sorted_ids,
                      block_expert, num_post_padded, cap_rows, nullptr, topk_weights, stage, ws,
                      ws_bytes, false, static_cast<cudaStream_t>(stream));
@@ -319,19 +382,27 @@ int moe_grouped_ffn(const void* x, const uint8_t* x_scale, int act_dt, const voi
                     const int32_t* block_expert, const int32_t* num_post_padded,
                     int64_t cap_rows, const float* topk_weights, void* stage, void* ws,
                     size_t ws_bytes, void* stream) {
-  (void)x_scale;
-  (void)w13_scale;
-  (void)w2_scale;
   int rc = check_ffn(act_dt, w_dt, T, H, F, E, k, block_m, cap_rows);
   if (rc != MOE_OK) return rc;
   if (T == 0) return MOE_OK;
-  if (!ws) return MOE_ERR_ARG;
+  if (!ws || !aligned(ws, 256)) return MOE_ERR_ARG;
   if (ws_bytes < moe_ffn_workspace_bytes(T, H, F, E, k, block_m, act_dt)) return MOE_ERR_ARG;
   if (cap_rows != static_cast<int64_t>(T) * k + static_cast<int64_t>(E) * (block_m - 1))
     return MOE_ERR_ARG;  // the workspace holds exactly the worst-case intermediate
-  const FfnLayout L = ffn_layout(T, F, E, k, block_m, true);
+  const FfnLayout L = ffn_layout(T, F, E, k, block_m, true, act_dt);
   void* inter = static_cast<char*>(ws) + kWsHeaderBytes + L.inter;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (act_dt == MOE_DT_E4M3) {
+    uint8_t* iq = static_cast<uint8_t*>(inter);
+    uint8_t* isc = iq + align_up(static_cast<size_t>(cap_rows) * F, 256);
+    rc = expert_gemm_lowbit(0, x, x_scale, w13, w13_scale, T, H, F, E, k, block_m, sorted_ids,
+                            block_expert, num_post_padded, cap_rows, iq, isc, nullptr, nullptr,
+                            ws, s);
+    if (rc != MOE_OK) return rc;
+    return expert_gemm_lowbit(1, iq, isc, w2, w2_scale, T, H, F, E, k, block_m, sorted_ids,
+                              block_expert, num_post_padded, cap_rows, nullptr, nullptr,
+                              topk_weights, stage, ws, s);
+  }
   rc = expert_gemm(0, x, act_dt, w13, w_dt, T, H, F, E, k, block_m, sorted_ids, block_expert,
                    num_post_padded, cap_rows, inter, nullptr, nullptr, ws, ws_bytes, true, s);
   if (rc != MOE_OK) return rc;
@@ -352,11 +423,10 @@ int moe_finalize(const void* stage, int T, int k, int H, void* out, void* stream
 
 // ---- layer ------------------------------------------------------------------------
 size_t moe_layer_workspace_bytes(int T, int H, int F, int E, int k, int block_m, int act_dt) {
-  (void)act_dt;
   if (T < 0 || H <= 0 || F <= 0 || E <= 0 || k <= 0) return 0;
   if (block_m == 0) block_m = moe_pick_block_m(T, k, E);
   if (check_block_m(block_m) != MOE_OK) return 0;
-  return layer_layout(T, H, F, E, k, block_m).total;
+  return layer_layout(T, H, F, E, k, block_m, act_dt).total;
 }
 
 int moe_layer(const void* hidden, int act_dt, const uint8_t* hidden_scale, const void* gate,
@@ -368,7 +438,7 @@ int moe_layer(const void* hidden, int act_dt, const uint8_t* hidden_scale, const
   int rc = check_router(hidden, act_dt, hidden_scale, gate, gate_dt, T, H, E, k, scoring,
                         n_group, topk_group);
   if (rc != MOE_OK) return rc;
-  const LayerLayout L = layer_layout(T, H, F, E, k, block_m);
+  const LayerLayout L = layer_layout(T, H, F, E, k, block_m, act_dt);
   rc = check_ffn(act_dt, w_dt, T, H, F, E, k, block_m, L.cap);
   if (rc != MOE_OK) return rc;
   if (T == 0) return MOE_OK;
@@ -391,8 +461,21 @@ int moe_layer(const void* hidden, int act_dt, const uint8_t* hidden_scale, const
     return launch_fail("router kernel");
   if (launch_align(ids, T, k, E, block_m, sorted, L.cap, blk, npp, err_word(ws), s) != 0)
     return launch_fail("align kernel");
-  const FfnLayout FL = ffn_layout(T, F, E, k, block_m, true);
+  const FfnLayout FL = ffn_layout(T, F, E, k, block_m, true, act_dt);
   void* inter = base + L.ffn + FL.inter;
+  if (act_dt == MOE_DT_E4M3) {
+    if (!hidden_scale || !w13_scale || !w2_scale) return MOE_ERR_ARG;
+    uint8_t* iq = static_cast<uint8_t*>(inter);
+    uint8_t* isc = iq + align_up(static_cast<size_t>(L.cap) * F, 256);
+    rc = expert_gemm_lowbit(0, hidden, hidden_scale, w13, w13_scale, T, H, F, E, k, block_m,
+                            sorted, blk, npp, L.cap, iq, isc, nullptr, nullptr, ws, s);
+    if (rc != MOE_OK) return rc;
+    rc = expert_gemm_lowbit(1, iq, isc, w2, w2_scale, T, H, F, E, k, block_m, sorted, blk, npp,
+                            L.cap, nullptr, nullptr, wts, stage, ws, s);
+    if (rc != MOE_OK) return rc;
+    if (launch_finalize(stage, T, k, H, out, s) != 0) return launch_fail("finalize kernel");
+    return MOE_OK;
+  }
   FfnParams p = ffn_params(T, H, F, E, k, block_m, sorted, blk, npp, L.cap, ws, L.ffn, FL);
   const int sms = device_num_sms();
   if (sms <= 0) return cuda_fail("cudaDeviceGetAttribute", cudaGetLastError());

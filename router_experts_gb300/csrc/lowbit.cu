@@ -1,0 +1,410 @@
+// lowbit.cu -- the expert GEMMs of the low-bit layer: FP8 e4m3 activations x
+// FP4 e2m1 weights, each with one UE8M0 scale per 32 values along K.
+//
+// Follows "How GPUs Fuse Communication and Computation During LLM Inference"
+// §1.1 (FP4 expert weights, FP8 token values, a scale per group of 32 values;
+// the output of GEMM 1 is re-quantised before GEMM 2 reads it) and §3.5 (the
+// GEMM 1 epilogue does SwiGLU and the re-quantisation: scale = the smallest
+// power of two with amax / scale <= 448, codes = fp8(act / scale)); the tile
+// scheme of "MoE Kernels, in depth" (expert from block_expert, rows from
+// sorted_ids, gather folded into the load, weight in the down GEMM's
+// epilogue).
+//
+// HBM traffic stays low-bit: converter warps read the packed codes and the
+// scale bytes, dequantise them exactly into f16 (every e2m1 / e4m3 value
+// times 2^u with u in [-14, 15] is an f16 number) in registers, and write the
+// 128-byte-swizzled operand tiles that a single thread feeds to
+// tcgen05.mma kind::f16 (f16 x f16 -> fp32 in TMEM; every product is exact).
+// 16 warps: warp 1 allocates TMEM and issues the MMAs, warps 2-9 convert
+// (one weight row and half a token row each per stage), warps 12-15 run the
+// epilogue; the others idle.  Tile: M = 128 token rows of one block (BLOCK_M
+// rows valid), N = 256 weight rows, K steps of 64, four stages, two
+// double-buffered 256-column accumulators.
+#include <cuda_fp4.h>
+#include <cuda_fp8.h>
+
+#include "moe_common.cuh"
+#include "moe_internal.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int kLbThreads = 512;
+constexpr int kLbStages = 4;
+constexpr int kLbA = 128 * 128;             // 128 token rows x 64 f16
+constexpr int kLbB = 256 * 128;             // 256 weight rows x 64 f16
+constexpr int kLbStage = kLbA + kLbB;       // 48 KB
+constexpr int kLbConv = 256;                // converter threads (warps 2-9)
+constexpr int kLbSmem = kLbStages * kLbStage + 1024 + 512;
+constexpr uint32_t kLbIdesc = (1u << 4) | (static_cast<uint32_t>(256 >> 3) << 17) |
+                              (static_cast<uint32_t>(128 >> 4) << 24);  // f16 x f16 -> f32
+
+// f16x2 holding 2^(code-127) twice (exponent clamped to the normal f16 range).
+MOE_DEV uint32_t scale_f16x2(uint32_t code) {
+  int e = static_cast<int>(code) - 127;
+  e = max(-14, min(15, e));
+  const uint32_t h = static_cast<uint32_t>(e + 15) << 10;
+  return h | (h << 16);
+}
+
+MOE_DEV uint32_t hmul2_u32(uint32_t a, uint32_t b) {
+  __half2 x = *reinterpret_cast<__half2*>(&a), y = *reinterpret_cast<__half2*>(&b);
+  __half2 r = __hmul2(x, y);
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+
+// 4 bytes = 8 e2m1 codes (low nibble first) -> 8 f16 (4 registers), scaled.
+MOE_DEV void fp4x8_to_f16(uint32_t w, uint32_t s2, uint32_t (&o)[4]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __nv_fp4x2_storage_t b = static_cast<__nv_fp4x2_storage_t>((w >> (8 * i)) & 0xFFu);
+    __half2_raw h = __nv_cvt_fp4x2_to_halfraw2(b, __NV_E2M1);
+    o[i] = hmul2_u32(*reinterpret_cast<uint32_t*>(&h), s2);
+  }
+}
+// 8 bytes = 8 e4m3 codes -> 8 f16 (4 registers), scaled.
+MOE_DEV void fp8x8_to_f16(uint32_t lo, uint32_t hi, uint32_t s2, uint32_t (&o)[4]) {
+  const uint32_t w[2] = {lo, hi};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __nv_fp8x2_storage_t b =
+        static_cast<__nv_fp8x2_storage_t>((w[i / 2] >> (16 * (i % 2))) & 0xFFFFu);
+    __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(b, __NV_E4M3);
+    o[i] = hmul2_u32(*reinterpret_cast<uint32_t*>(&h), s2);
+  }
+}
+
+MOE_DEV void st_shared_v4(uint32_t addr, const uint32_t (&v)[4]) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v[0]), "r"(v[1]),
+               "r"(v[2]), "r"(v[3])
+               : "memory");
+}
+
+struct LbUnit {
+  int b, n, e;
+};
+
+// The raw bytes one converter thread reads for one K step.
+struct LbRaw {
+  uint4 w0, w1;     // 64 e2m1 codes of the weight row
+  uint32_t wsc;     // its two scale bytes (low = first 32)
+  uint4 t0, t1;     // 32 e4m3 codes of half a token row
+  uint32_t tsc;     // its scale byte
+  bool wvalid, tvalid;
+};
+
+template <int KIND>
+MOE_DEV void lb_load(const LowbitParams& p, const LbUnit& u, int kb, int ct, int K,
+                     LbRaw& r) {
+  // weight row ct of the tile
+  int wrow;
+  bool wv;
+  if constexpr (KIND == 0) {
+    const int fr = u.n * 128 + (ct & 127);
+    wv = fr < p.F;
+    wrow = u.e * 2 * p.F + ((ct < 128) ? 0 : p.F) + fr;
+  } else {
+    const int hr = u.n * 256 + ct;
+    wv = hr < p.H;
+    wrow = u.e * p.H + hr;
+  }
+  r.wvalid = wv;
+  if (wv) {
+    const uint4* src = reinterpret_cast<const uint4*>(
+        p.w + static_cast<size_t>(wrow) * (K / 2) + static_cast<size_t>(kb) * 32);
+    r.w0 = __ldg(src);
+    r.w1 = __ldg(src + 1);
+    r.wsc = __ldg(reinterpret_cast<const uint16_t*>(
+        p.w_scale + static_cast<size_t>(wrow) * (K / 32) + static_cast<size_t>(kb) * 2));
+  }
+  // half (ct & 1) of token row ct >> 1
+  const int tr = ct >> 1, half = ct & 1;
+  r.tvalid = false;
+  if (tr < p.BM) {
+    const size_t prow = static_cast<size_t>(u.b) * p.BM + tr;
+    const uint8_t* base = nullptr;
+    const uint8_t* sbase = nullptr;
+    if constexpr (KIND == 0) {
+      const int a = __ldg(p.sorted_ids + prow);
+      if (a >= 0 && a < p.T * p.k) {
+        const size_t tok = static_cast<size_t>(a / p.k);
+        base = p.act + tok * K;
+        sbase = p.act_scale + tok * (K / 32);
+      }
+    } else {
+      base = p.act + prow * K;
+      sbase = p.act_scale + prow * (K / 32);
+    }
+    if (base) {
+      const uint4* src =
+          reinterpret_cast<const uint4*>(base + static_cast<size_t>(kb) * 64 + half * 32);
+      r.t0 = __ldg(src);
+      r.t1 = __ldg(src + 1);
+      r.tsc = __ldg(sbase + static_cast<size_t>(kb) * 2 + half);
+      r.tvalid = true;
+    }
+  }
+}
+
+// Dequantise one K step into the swizzled f16 operand tiles of a stage.
+MOE_DEV void lb_store(const LbRaw& r, int ct, int BM, uint32_t a_tile, uint32_t b_tile) {
+  {
+    const uint32_t row = ct;
+    const uint32_t s_lo = scale_f16x2(r.wsc & 0xFFu), s_hi = scale_f16x2((r.wsc >> 8) & 0xFFu);
+    const uint32_t words[8] = {r.w0.x, r.w0.y, r.w0.z, r.w0.w, r.w1.x, r.w1.y, r.w1.z, r.w1.w};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      uint32_t o[4] = {0u, 0u, 0u, 0u};
+      if (r.wvalid) fp4x8_to_f16(words[j], j < 4 ? s_lo : s_hi, o);
+      const uint32_t dst = b_tile + row * 128 + ((j ^ (row & 7)) << 4);
+      st_shared_v4(dst, o);
+    }
+  }
+  const int tr = ct >> 1, half = ct & 1;
+  if (tr < BM) {
+    const uint32_t s2 = scale_f16x2(r.tsc);
+    const uint32_t words[8] = {r.t0.x, r.t0.y, r.t0.z, r.t0.w, r.t1.x, r.t1.y, r.t1.z, r.t1.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      uint32_t o[4] = {0u, 0u, 0u, 0u};
+      if (r.tvalid) fp8x8_to_f16(words[2 * j], words[2 * j + 1], s2, o);
+      const int chunk = half * 4 + j;
+      const uint32_t dst = a_tile + tr * 128 + ((chunk ^ (tr & 7)) << 4);
+      st_shared_v4(dst, o);
+    }
+  }
+}
+
+// e4m3 codes of 32 activations with their UE8M0 exponent byte: scale = the
+// smallest power of two 2^s with amax <= 448 * 2^s (2^0 when all are zero).
+MOE_DEV uint32_t requant32(const float (&v)[32], uint32_t (&codes)[8]) {
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  int s = 0;
+  if (amax > 0.f) {
+    // ceil(log2(amax / 448)) from the bits of the fp32 quotient
+    const float q = amax / 448.0f;
+    const uint32_t bits = __float_as_uint(q);
+    s = static_cast<int>((bits >> 23) & 0xFFu) - 127 + ((bits & 0x7FFFFFu) ? 1 : 0);
+    s = max(-127, min(127, s));
+  }
+  const float inv = exp2f(static_cast<float>(-s));
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const __nv_fp8x2_storage_t lo =
+        __nv_cvt_float2_to_fp8x2(make_float2(v[4 * i] * inv, v[4 * i + 1] * inv), __NV_SATFINITE,
+                                 __NV_E4M3);
+    const __nv_fp8x2_storage_t hi =
+        __nv_cvt_float2_to_fp8x2(make_float2(v[4 * i + 2] * inv, v[4 * i + 3] * inv),
+                                 __NV_SATFINITE, __NV_E4M3);
+    codes[i] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+  }
+  return static_cast<uint32_t>(s + 127);
+}
+
+template <int KIND>
+__global__ void __launch_bounds__(kLbThreads, 1) lowbit_gemm_kernel(const LowbitParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + kLbStages * kLbStage);
+  uint64_t* empty_bar = full_bar + kLbStages;
+  uint64_t* tfull_bar = empty_bar + kLbStages;
+  uint64_t* tempty_bar = tfull_bar + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty_bar + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int K = (KIND == 0) ? p.H : p.F;
+  const int KB = K / 64;
+  int npp = __ldg(p.num_post_padded);
+  npp = max(0, min(npp, p.cap_rows));
+  const int nblk = npp / p.BM;
+  const int ntiles = (KIND == 0) ? (p.F + 127) / 128 : (p.H + 255) / 256;
+  const int num_units = nblk * ntiles;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kLbStages; ++i) {
+      mbar_init(&full_bar[i], kLbConv);
+      mbar_init(&empty_bar[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&tfull_bar[i], 1);
+      mbar_init(&tempty_bar[i], 4);
+    }
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  auto decode = [&](int uu) {
+    LbUnit u;
+    u.b = uu / ntiles;
+    u.n = uu % ntiles;
+    int e = __ldg(p.block_expert + u.b);
+    if (e < 0 || e >= p.E) {
+      if (threadIdx.x == 0) raise_error(p.err, kErrBadTable);
+      e = min(max(e, 0), p.E - 1);
+    }
+    u.e = e;
+    return u;
+  };
+
+  if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      uint32_t it = 0, acc_it = 0;
+      bool alive = true;
+      for (int uu = blockIdx.x; alive && uu < num_units; uu += gridDim.x, ++acc_it) {
+        const int buf = acc_it & 1;
+        const uint32_t aph = (acc_it >> 1) & 1u;
+        if (!mbar_wait(&tempty_bar[buf], aph ^ 1u, abort_flag, p.err)) break;
+        tc_fence_after();
+        const uint32_t d = tmem_base + buf * 256;
+        for (int kb = 0; kb < KB; ++kb, ++it) {
+          const int st = it % kLbStages;
+          const uint32_t ph = (it / kLbStages) & 1u;
+          if (!mbar_wait(&full_bar[st], ph, abort_flag, p.err)) {
+            alive = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(smem + st * kLbStage);
+          const uint32_t b_addr = a_addr + kLbA;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            umma_f16(d, sw128_desc(a_addr + kk * 32), sw128_desc(b_addr + kk * 32), kLbIdesc,
+                     (kb > 0 || kk > 0) ? 1u : 0u);
+          umma_commit(&empty_bar[st]);
+        }
+        if (!alive) break;
+        umma_commit(&tfull_bar[buf]);
+      }
+    }
+  } else if (warp >= 2 && warp < 10) {
+    // ---------------- converters ----------------
+    const int ct = threadIdx.x - 64;  // 0..255
+    uint32_t it = 0;
+    bool alive = true;
+    for (int uu = blockIdx.x; alive && uu < num_units; uu += gridDim.x) {
+      const LbUnit u = decode(uu);
+      LbRaw cur, nxt;
+      lb_load<KIND>(p, u, 0, ct, K, cur);
+      for (int kb = 0; kb < KB; ++kb, ++it) {
+        if (kb + 1 < KB) lb_load<KIND>(p, u, kb + 1, ct, K, nxt);
+        const int st = it % kLbStages;
+        const uint32_t ph = (it / kLbStages) & 1u;
+        if (!mbar_wait(&empty_bar[st], ph ^ 1u, abort_flag, p.err)) {
+          alive = false;
+          break;
+        }
+        const uint32_t a_tile = smem_u32(smem + st * kLbStage);
+        lb_store(cur, ct, p.BM, a_tile, a_tile + kLbA);
+        fence_proxy_async_smem();  // generic-proxy tile writes -> tensor core reads
+        mbar_arrive(&full_bar[st]);
+        cur = nxt;
+      }
+    }
+  } else if (warp >= 12) {
+    // ---------------- epilogue ----------------
+    const int ew = warp - 12;
+    const int row = ew * 32 + lane;
+    uint32_t acc_it = 0;
+    for (int uu = blockIdx.x; uu < num_units; uu += gridDim.x, ++acc_it) {
+      const LbUnit u = decode(uu);
+      const int buf = acc_it & 1;
+      const uint32_t aph = (acc_it >> 1) & 1u;
+      const bool ok = mbar_wait(&tfull_bar[buf], aph, abort_flag, p.err);
+      if (named_bar_any(1, 128, !ok || *abort_flag)) break;
+      tc_fence_after();
+      const uint32_t tb = tmem_base + (static_cast<uint32_t>(ew * 32) << 16) + buf * 256;
+      const bool rvalid = row < p.BM;
+      const size_t prow = static_cast<size_t>(u.b) * p.BM + row;
+      if constexpr (KIND == 0) {
+        // SwiGLU of gate column c and up column 128 + c, re-quantised per 32
+#pragma unroll 1
+        for (int j = 0; j < 4; ++j) {
+          uint32_t g0[16], g1[16], u0[16], u1[16];
+          tmem_ld16(tb + 32 * j, g0);
+          tmem_ld16(tb + 32 * j + 16, g1);
+          tmem_ld16(tb + 128 + 32 * j, u0);
+          tmem_ld16(tb + 128 + 32 * j + 16, u1);
+          tmem_ld_wait();
+          reg_fence16(g0);
+          reg_fence16(g1);
+          reg_fence16(u0);
+          reg_fence16(u1);
+          float act[32];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            act[i] = swiglu_f(__uint_as_float(g0[i]), __uint_as_float(u0[i]));
+            act[16 + i] = swiglu_f(__uint_as_float(g1[i]), __uint_as_float(u1[i]));
+          }
+          uint32_t codes[8];
+          const uint32_t sbyte = requant32(act, codes);
+          const int f = u.n * 128 + 32 * j;
+          if (rvalid && f + 32 <= p.F) {
+            st_global_v8(p.inter_q + prow * p.F + f, codes);
+            p.inter_scale[prow * (p.F / 32) + f / 32] = static_cast<uint8_t>(sbyte);
+          }
+        }
+      } else {
+        int a = p.T * p.k;
+        if (rvalid) a = __ldg(p.sorted_ids + prow);
+        const bool valid = rvalid && a >= 0 && a < p.T * p.k;
+        const float w = valid ? __ldg(p.topk_weights + a) : 0.f;
+#pragma unroll 1
+        for (int c = 0; c < 16; ++c) {
+          uint32_t r[16];
+          tmem_ld16(tb + 16 * c, r);
+          tmem_ld_wait();
+          reg_fence16(r);
+          const int h = u.n * 256 + 16 * c;
+          if (valid && h + 16 <= p.H) {
+            uint32_t o[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              o[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * w, __uint_as_float(r[2 * i + 1]) * w);
+            st_global_v8(p.stage + static_cast<size_t>(a) * p.H + h, o);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty_bar[buf]);
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, 512);
+  }
+}
+
+}  // namespace
+
+int launch_lowbit_gemm(int kind, const LowbitParams& p, int num_sms, cudaStream_t stream) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(lowbit_gemm_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kLbSmem) != cudaSuccess ||
+        cudaFuncSetAttribute(lowbit_gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kLbSmem) != cudaSuccess)
+      return -1;
+    attr_set = true;
+  }
+  if (kind == 0)
+    lowbit_gemm_kernel<0><<<num_sms, kLbThreads, kLbSmem, stream>>>(p);
+  else
+    lowbit_gemm_kernel<1><<<num_sms, kLbThreads, kLbSmem, stream>>>(p);
+  return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
+
+}  // namespace moe

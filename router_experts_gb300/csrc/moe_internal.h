@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -62,6 +63,25 @@ size_t ffn_partial_bytes(int block_m);
 // kind 0: GEMM1 + SwiGLU, kind 1: GEMM2 + routing weight.
 int launch_ffn_gemm(int kind, int block_m, const void* w, const FfnParams& p, int num_sms,
                     cudaStream_t stream, const char** why);
+
+// ---- low-bit expert GEMMs (e4m3 activations x e2m1 weights, UE8M0 per 32) ------
+struct LowbitParams {
+  const int32_t* sorted_ids;
+  const int32_t* block_expert;
+  const int32_t* num_post_padded;
+  const uint8_t* act;          // GEMM1: x codes [T, H]; GEMM2: inter codes [cap, F]
+  const uint8_t* act_scale;    // GEMM1: [T, H/32]; GEMM2: [cap, F/32]
+  const uint8_t* w;            // GEMM1: w13 [E*2F, H/2]; GEMM2: w2 [E*H, F/2]
+  const uint8_t* w_scale;      // GEMM1: [E*2F, H/32]; GEMM2: [E*H, F/32]
+  uint8_t* inter_q;            // GEMM1 output codes [cap, F]
+  uint8_t* inter_scale;        // GEMM1 output scales [cap, F/32]
+  const float* topk_weights;   // GEMM2 row weights [T*k]
+  __nv_bfloat16* stage;        // GEMM2 output [T*k, H]
+  int* err;
+  int T, H, F, E, k, BM;
+  int cap_rows;
+};
+int launch_lowbit_gemm(int kind, const LowbitParams& p, int num_sms, cudaStream_t stream);
 
 // ---- finalize -----------------------------------------------------------------
 int launch_finalize(const void* stage, int T, int k, int H, void* out, cudaStream_t stream);

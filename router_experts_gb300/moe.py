@@ -181,56 +181,70 @@ def _wdt(w):
     return DT_BF16 if w.dtype == torch.bfloat16 else DT_E2M1
 
 
+def _is_lowbit(w):
+    return w.dtype == torch.uint8
+
+
 def expert_gemm1(x, w13, block_m, sorted_ids, block_expert, npp, k, cap_rows=None,
-                 ws: Workspace | None = None):
-    """-> inter [cap, F] bf16."""
+                 ws: Workspace | None = None, x_scale=None, w13_scale=None):
+    """bf16: -> inter [cap, F] bf16.  Low-bit (uint8 e4m3 x with x_scale, packed
+    e2m1 w13 with w13_scale): -> (inter codes [cap, F] uint8, scales [cap, F/32])."""
     lib = load()
     T, H = x.shape
     E, F2, _ = w13.shape
     F = F2 // 2
     cap = sorted_ids.numel() if cap_rows is None else int(cap_rows)
-    inter = torch.empty((cap, F), dtype=torch.bfloat16, device=x.device)
+    act_dt = _dt(x, x_scale)
     ws = ws or default_workspace(x.device)
-    buf = ws.get(lib.moe_ffn_workspace_bytes(T, H, F, E, k, block_m, _dt(x, None)))
-    rc = lib.moe_expert_gemm1(_p(x), _dt(x, None), None, _p(w13), None, _wdt(w13), T, H, F, E, k,
-                              block_m, _p(sorted_ids), _p(block_expert), _p(npp), cap, _p(inter),
-                              None, _p(buf), buf.numel(), _stream(x.device))
+    buf = ws.get(lib.moe_ffn_workspace_bytes(T, H, F, E, k, block_m, act_dt))
+    if act_dt == DT_E4M3:
+        inter = torch.empty((cap, F), dtype=torch.uint8, device=x.device)
+        isc = torch.empty((cap, F // 32), dtype=torch.uint8, device=x.device)
+    else:
+        inter = torch.empty((cap, F), dtype=torch.bfloat16, device=x.device)
+        isc = None
+    rc = lib.moe_expert_gemm1(_p(x), act_dt, _p(x_scale), _p(w13), _p(w13_scale), _wdt(w13), T, H,
+                              F, E, k, block_m, _p(sorted_ids), _p(block_expert), _p(npp), cap,
+                              _p(inter), _p(isc), _p(buf), buf.numel(), _stream(x.device))
     _check(rc, "moe_expert_gemm1")
-    return inter
+    return (inter, isc) if act_dt == DT_E4M3 else inter
 
 
 def expert_gemm2(inter, w2, T, k, block_m, sorted_ids, block_expert, npp, topk_weights,
-                 ws: Workspace | None = None):
+                 ws: Workspace | None = None, inter_scale=None, w2_scale=None):
     """-> stage [T*k, H] bf16 (rows weighted by topk_weights)."""
     lib = load()
-    E, H, F = w2.shape
+    E, H, Fw = w2.shape
+    F = Fw * 2 if _is_lowbit(w2) else Fw
     cap = inter.shape[0]
+    act_dt = DT_E4M3 if inter_scale is not None else DT_BF16
     stage = torch.empty((T * k, H), dtype=torch.bfloat16, device=inter.device)
     ws = ws or default_workspace(inter.device)
-    buf = ws.get(lib.moe_ffn_workspace_bytes(T, H, F, E, k, block_m, DT_BF16))
-    rc = lib.moe_expert_gemm2(_p(inter), None, DT_BF16, _p(w2), None, _wdt(w2), T, H, F, E, k,
-                              block_m, _p(sorted_ids), _p(block_expert), _p(npp), cap,
-                              _p(topk_weights), _p(stage), _p(buf), buf.numel(),
+    buf = ws.get(lib.moe_ffn_workspace_bytes(T, H, F, E, k, block_m, act_dt))
+    rc = lib.moe_expert_gemm2(_p(inter), _p(inter_scale), act_dt, _p(w2), _p(w2_scale), _wdt(w2),
+                              T, H, F, E, k, block_m, _p(sorted_ids), _p(block_expert), _p(npp),
+                              cap, _p(topk_weights), _p(stage), _p(buf), buf.numel(),
                               _stream(inter.device))
     _check(rc, "moe_expert_gemm2")
     return stage
 
 
 def grouped_ffn(x, w13, w2, k, block_m, sorted_ids, block_expert, npp, topk_weights,
-                ws: Workspace | None = None):
+                ws: Workspace | None = None, x_scale=None, w13_scale=None, w2_scale=None):
     """GEMM1 + SwiGLU and GEMM2 + weight -> stage [T*k, H] bf16."""
     lib = load()
     T, H = x.shape
     E, F2, _ = w13.shape
     F = F2 // 2
     cap = sorted_ids.numel()
+    act_dt = _dt(x, x_scale)
     stage = torch.empty((T * k, H), dtype=torch.bfloat16, device=x.device)
     ws = ws or default_workspace(x.device)
-    buf = ws.get(lib.moe_ffn_workspace_bytes(T, H, F, E, k, block_m, _dt(x, None)))
-    rc = lib.moe_grouped_ffn(_p(x), None, _dt(x, None), _p(w13), None, _p(w2), None, _wdt(w13),
-                             T, H, F, E, k, block_m, _p(sorted_ids), _p(block_expert), _p(npp),
-                             cap, _p(topk_weights), _p(stage), _p(buf), buf.numel(),
-                             _stream(x.device))
+    buf = ws.get(lib.moe_ffn_workspace_bytes(T, H, F, E, k, block_m, act_dt))
+    rc = lib.moe_grouped_ffn(_p(x), _p(x_scale), act_dt, _p(w13), _p(w13_scale), _p(w2),
+                             _p(w2_scale), _wdt(w13), T, H, F, E, k, block_m, _p(sorted_ids),
+                             _p(block_expert), _p(npp), cap, _p(topk_weights), _p(stage),
+                             _p(buf), buf.numel(), _stream(x.device))
     _check(rc, "moe_grouped_ffn")
     return stage
 
@@ -256,7 +270,7 @@ def layer(hidden, gate, bias, w13, w2, k, scoring="softmax", n_group=1, topk_gro
     lib = load()
     T = hidden.shape[0]
     E, H = gate.shape
-    F = w2.shape[2] * (2 if w2.dtype == torch.uint8 else 1)
+    F = w2.shape[2] * (2 if _is_lowbit(w2) else 1)
     act_dt = _dt(hidden, hidden_scale)
     dev = hidden.device
     out = torch.empty((T, H), dtype=torch.bfloat16, device=dev) if out is None else out

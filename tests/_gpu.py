@@ -31,16 +31,20 @@ def oracle_router(oracle, w, d, T, tokens):
                          x_scale=host(d.get("hidden_scale")), tokens=tokens)
 
 
-def compact_experts(w13, w2, ids_rows):
+def compact_experts(w13, w2, ids_rows, w13_scale=None, w2_scale=None):
     """Host copies of only the experts the sampled rows use, with ids remapped
-    (keeps the oracle's input small for the 22.5 GB workload)."""
+    (keeps the oracle's input small for the 22.5 GB workload).  With scales
+    (low-bit weights) returns (w13, w2, ids, n, w13_scale, w2_scale)."""
     used = np.unique(ids_rows.reshape(-1))
     remap = {int(e): i for i, e in enumerate(used)}
     idx = torch.as_tensor(used, dtype=torch.long, device=w13.device)
     w13h = host(w13.index_select(0, idx))
     w2h = host(w2.index_select(0, idx))
     new_ids = np.array([[remap[int(e)] for e in r] for r in ids_rows], dtype=np.int32).reshape(ids_rows.shape)
-    return w13h, w2h, new_ids, len(used)
+    if w13_scale is None:
+        return w13h, w2h, new_ids, len(used)
+    return (w13h, w2h, new_ids, len(used), host(w13_scale.index_select(0, idx)),
+            host(w2_scale.index_select(0, idx)))
 
 
 def rel_err(got, ref):

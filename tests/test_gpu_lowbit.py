@@ -1,0 +1,105 @@
+"""Low-bit expert path (FP8 e4m3 activations x FP4 e2m1 weights, one UE8M0
+scale per 32 values; "How GPUs Fuse Communication and Computation During LLM
+Inference" §1.1, §3.5) against the oracle fed the same dequantised values:
+max|err| <= 6e-2 * max|ref| for the layer.  Also checked against the oracle's
+emulation of the e4m3 re-quantisation of the intermediate, which the GPU path
+performs, with a tighter bound."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from router_experts_gb300 import moe
+from router_experts_gb300 import workloads as W
+
+from _gpu import GAP_MIN, LAYER_RTOL_LOWBIT, compact_experts, host, oracle_router, rel_err, \
+    sample_tokens
+
+pytestmark = pytest.mark.gpu
+
+_CACHE = {}
+
+
+def v4lo_inputs(T, seed):
+    key = (T, seed)
+    if key not in _CACHE:
+        _CACHE.clear()
+        torch.cuda.empty_cache()
+        _CACHE[key] = W.make_inputs(W.WORKLOADS["v4lo"], T, seed=seed, device="cuda")
+    return _CACHE[key]
+
+
+def oracle_ffn_lowbit(d, tokens, ids_rows, w_rows, w, emulate=0):
+    w13h, w2h, rid, En, s13, s2 = compact_experts(d["w13"], d["w2"], ids_rows, d["w13_scale"],
+                                                  d["w2_scale"])
+    xh = host(d["hidden"])[tokens]
+    xs = host(d["hidden_scale"])[tokens]
+    return oracle.moe_ffn(xh, "e4m3", w13h, w2h, "e2m1", len(tokens), w.H, w.F, En, w.k, rid,
+                          np.asarray(w_rows, np.float64), x_scale=xs, w13_scale=s13,
+                          w2_scale=s2, emulate=emulate)
+
+
+@pytest.mark.parametrize("T", [64, 512, 4096])
+def test_lowbit_ffn_matches_oracle(T):
+    w = W.WORKLOADS["v4lo"]
+    d = v4lo_inputs(T, seed=2)
+    ids, wts = W.random_routing(T, w.k, w.E, seed=T)
+    BM = moe.pick_block_m(T, w.k, w.E)
+    s, b, npp = moe.align(ids.cuda(), w.E, BM)
+    stage = moe.grouped_ffn(d["hidden"], d["w13"], d["w2"], w.k, BM, s, b, npp, wts.cuda(),
+                            x_scale=d["hidden_scale"], w13_scale=d["w13_scale"],
+                            w2_scale=d["w2_scale"])
+    y = moe.finalize(stage, T, w.k)
+    torch.cuda.synchronize()
+    tokens = sample_tokens(T, 12, seed=T)
+    got = y.float().cpu().numpy()[tokens]
+    ref = oracle_ffn_lowbit(d, tokens, ids.numpy()[tokens], wts.numpy()[tokens], w)
+    err = rel_err(got, ref)
+    emu = oracle_ffn_lowbit(d, tokens, ids.numpy()[tokens], wts.numpy()[tokens], w, emulate=2)
+    err_emu = rel_err(got, emu)
+    print(f"low-bit ffn T={T} BM={BM}: rel err {err:.2e} (vs exact), {err_emu:.2e} (vs emulated "
+          f"re-quantisation)")
+    assert np.isfinite(got).all()
+    assert err <= LAYER_RTOL_LOWBIT
+    assert err_emu <= 2e-2
+
+
+def test_lowbit_gemm_entry_points_compose():
+    w = W.WORKLOADS["v4lo"]
+    T = 64
+    d = v4lo_inputs(T, seed=3)
+    ids, wts = W.random_routing(T, w.k, w.E, seed=5)
+    BM = moe.pick_block_m(T, w.k, w.E)
+    s, b, npp = moe.align(ids.cuda(), w.E, BM)
+    iq, isc = moe.expert_gemm1(d["hidden"], d["w13"], BM, s, b, npp, w.k,
+                               x_scale=d["hidden_scale"], w13_scale=d["w13_scale"])
+    st1 = moe.expert_gemm2(iq, d["w2"], T, w.k, BM, s, b, npp, wts.cuda(), inter_scale=isc,
+                           w2_scale=d["w2_scale"])
+    st2 = moe.grouped_ffn(d["hidden"], d["w13"], d["w2"], w.k, BM, s, b, npp, wts.cuda(),
+                          x_scale=d["hidden_scale"], w13_scale=d["w13_scale"],
+                          w2_scale=d["w2_scale"])
+    torch.cuda.synchronize()
+    assert torch.equal(st1, st2)
+    # the intermediate scales are powers of two bounding every 32-block
+    codes = iq[: int(npp.item())].cpu()
+    assert codes.dtype == torch.uint8 and isc.dtype == torch.uint8
+
+
+@pytest.mark.parametrize("T,ntok", [(512, 12), (4096, 12)])
+def test_lowbit_layer_matches_oracle(T, ntok):
+    w = W.WORKLOADS["v4lo"]
+    d = v4lo_inputs(T, seed=0)
+    y = moe.layer(d["hidden"], d["gate"], d["bias"], d["w13"], d["w2"], w.k, w.scoring,
+                  renormalize=w.renormalize, scaling=w.scaling, hidden_scale=d["hidden_scale"],
+                  w13_scale=d["w13_scale"], w2_scale=d["w2_scale"])
+    torch.cuda.synchronize()
+    tokens = sample_tokens(T, ntok, seed=T)
+    ids_o, w_o, gap = oracle_router(oracle, w, d, T, tokens)
+    keep = gap > GAP_MIN
+    tokens, ids_o, w_o = tokens[keep], ids_o[keep], w_o[keep]
+    ref = oracle_ffn_lowbit(d, tokens, ids_o, w_o, w)
+    got = y.float().cpu().numpy()[tokens]
+    err = rel_err(got, ref)
+    print(f"low-bit layer T={T}: {len(tokens)} tokens, rel err {err:.2e}")
+    assert len(tokens) > 0 and np.isfinite(got).all()
+    assert err <= LAYER_RTOL_LOWBIT
