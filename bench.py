@@ -149,15 +149,25 @@ def barrier(world: int, device=None):
 # --------------------------------------------------------------------------
 # algorithmic bytes / FLOPs (the method's own, padding and round trips apart)
 # --------------------------------------------------------------------------
-def work_model(w, T, touched, block_m, b_x=2, b_w=2, b_g=2):
+def work_model(w, T, touched, block_m, b_x=None, b_w=None, b_g=None):
+    """Bytes per element: bf16 2; low-bit workload: e4m3 activations and the
+    re-quantised intermediate 1 + 1/32 (scale byte per 32), e2m1 weights
+    0.5 + 1/32, fp32 gate 4."""
     H, E, k, F = w.H, w.E, w.k, w.F
+    if b_x is None:
+        b_x = (1 + 1 / 32) if w.lowbit else 2
+    if b_w is None:
+        b_w = (0.5 + 1 / 32) if w.lowbit else 2
+    if b_g is None:
+        b_g = 4 if w.lowbit else 2
+    b_i = (1 + 1 / 32) if w.lowbit else 2   # intermediate
     cap = T * k + E * (block_m - 1)
     st = {
         "router": {"bytes": E * H * b_g + T * H * b_x + 8 * T * k, "flops": 2 * T * E * H},
         "align": {"bytes": 4 * T * k + 4 * cap + 4 * math.ceil(cap / block_m), "flops": 0},
-        "gemm1": {"bytes": touched * 2 * F * H * b_w + T * H * b_x + T * k * F * 2,
+        "gemm1": {"bytes": touched * 2 * F * H * b_w + T * H * b_x + T * k * F * b_i,
                   "flops": 2 * T * k * 2 * F * H},
-        "gemm2": {"bytes": touched * H * F * b_w + T * k * F * 2 + T * k * H * 2,
+        "gemm2": {"bytes": touched * H * F * b_w + T * k * F * b_i + T * k * H * 2,
                   "flops": 2 * T * k * H * F},
         "finalize": {"bytes": T * k * H * 2 + T * H * 2, "flops": 0},
     }
@@ -256,16 +266,29 @@ def run_ours(args):
     ws = moe.Workspace(dev)
     names = ["router", "align", "gemm1", "gemm2", "finalize"]
 
-    def stage_graphs(x):
-        """One CUDA graph per kernel for the batch x; returns graphs + routing facts."""
+    def stage_graphs(x, xs=None):
+        """One CUDA graph per kernel for the batch x (xs: its scales for the
+        low-bit workload); returns graphs + routing facts."""
         Tn = x.shape[0]
         bm = moe.pick_block_m(Tn, k, E)
         a_r = (x, d["gate"], d.get("bias"), k, w.scoring, w.n_group, w.topk_group,
                w.renormalize, w.scaling)
-        ids, wts = moe.router(*a_r, ws=ws)
+        lb = dict(x_scale=xs, w13_scale=d.get("w13_scale")) if w.lowbit else {}
+        lb2 = dict(w2_scale=d.get("w2_scale")) if w.lowbit else {}
+
+        def g1(s_ids, blk, npp):
+            return moe.expert_gemm1(x, d["w13"], bm, s_ids, blk, npp, k, ws=ws, **lb)
+
+        def g2(inter, s_ids, blk, npp):
+            if w.lowbit:
+                return moe.expert_gemm2(inter[0], d["w2"], Tn, k, bm, s_ids, blk, npp, wts, ws=ws,
+                                        inter_scale=inter[1], **lb2)
+            return moe.expert_gemm2(inter, d["w2"], Tn, k, bm, s_ids, blk, npp, wts, ws=ws)
+
+        ids, wts = moe.router(*a_r, hidden_scale=xs, ws=ws)
         s_ids, blk, npp = moe.align(ids, E, bm, ws=ws)
-        inter = moe.expert_gemm1(x, d["w13"], bm, s_ids, blk, npp, k, ws=ws)
-        st = moe.expert_gemm2(inter, d["w2"], Tn, k, bm, s_ids, blk, npp, wts, ws=ws)
+        inter = g1(s_ids, blk, npp)
+        st = g2(inter, s_ids, blk, npp)
         y = moe.finalize(st, Tn, k)
         torch.cuda.synchronize()
         gs, outs = {}, {}
@@ -276,12 +299,12 @@ def run_ours(args):
                 outs[name] = fn()
             gs[name] = g
 
-        cap("router", lambda: moe.router(*a_r, ws=ws, out=(ids, wts)))
+        cap("router", lambda: moe.router(*a_r, hidden_scale=xs, ws=ws, out=(ids, wts)))
         cap("align", lambda: moe.align(ids, E, bm, ws=ws))
         s2, b2, n2 = outs["align"]
-        cap("gemm1", lambda: moe.expert_gemm1(x, d["w13"], bm, s2, b2, n2, k, ws=ws))
+        cap("gemm1", lambda: g1(s2, b2, n2))
         i2 = outs["gemm1"]
-        cap("gemm2", lambda: moe.expert_gemm2(i2, d["w2"], Tn, k, bm, s2, b2, n2, wts, ws=ws))
+        cap("gemm2", lambda: g2(i2, s2, b2, n2))
         st2 = outs["gemm2"]
         cap("finalize", lambda: moe.finalize(st2, Tn, k, out=y))
         for n in names:
@@ -292,10 +315,12 @@ def run_ours(args):
                  "padded_rows": int(n2.item())}
         return gs, facts, outs
 
-    graphs, facts, keep_alive = stage_graphs(d["hidden"])
+    graphs, facts, keep_alive = stage_graphs(d["hidden"], d.get("hidden_scale"))
     BM, touched = facts["block_m"], facts["touched"]
 
     weights_bytes = (d["w13"].numel() + d["w2"].numel()) * d["w13"].element_size()
+    lbk = dict(hidden_scale=d.get("hidden_scale"), w13_scale=d.get("w13_scale"),
+               w2_scale=d.get("w2_scale")) if w.lowbit else {}
     l2_note = ("inputs larger than L2 (expert weights %.2f GB)" % (weights_bytes / 1e9)
                if weights_bytes > 256e6 else "L2 flushed between steps")
     flush = None if weights_bytes > 256e6 else torch.empty(512 << 20, dtype=torch.uint8,
@@ -348,8 +373,10 @@ def run_ours(args):
     st_model, layer_model = work_model(w, T, touched, BM)
     dom = max(names, key=lambda n: stage_ms[n])
     roof = roofline_of(st_model[dom]["bytes"], st_model[dom]["flops"], stage_ms[dom] / 1e3, peaks)
+    gk = ("lowbit_gemm_kernel<%d>", "lowbit_gemm_kernel<%d>") if w.lowbit else \
+        ("ffn_gemm_kernel<%d," + str(BM) + ">", "ffn_gemm_kernel<%d," + str(BM) + ">")
     roof["kernel"] = {"router": "router_kernel", "align": "align_kernel",
-                      "gemm1": "ffn_gemm_kernel<0,%d>" % BM, "gemm2": "ffn_gemm_kernel<1,%d>" % BM,
+                      "gemm1": gk[0] % 0, "gemm2": gk[1] % 1,
                       "finalize": "finalize_kernel"}[dom]
     roof["traffic"] = None
     roof["peak_source"] = peaks["source"] + " (burst)"
@@ -364,7 +391,9 @@ def run_ours(args):
             if Ts >= T:
                 continue
             xs = d["hidden"][:Ts].contiguous()
-            gs, fs, ka = stage_graphs(xs)
+            xsc = d["hidden_scale"][:Ts].contiguous() if w.lowbit else None
+            gs, fs, ka = stage_graphs(xs, xsc)
+            lbs = dict(lbk, hidden_scale=xsc) if w.lowbit else {}
             times = {n: [] for n in names}
             for it in range(25):
                 fl.zero_()
@@ -381,10 +410,10 @@ def run_ours(args):
             # the layer as a user runs it: one graph holding the five kernels
             lg = torch.cuda.CUDAGraph()
             moe.layer(xs, d["gate"], d.get("bias"), d["w13"], d["w2"], k, w.scoring, w.n_group,
-                      w.topk_group, w.renormalize, w.scaling, ws=ws)
+                      w.topk_group, w.renormalize, w.scaling, ws=ws, **lbs)
             with torch.cuda.graph(lg):
                 moe.layer(xs, d["gate"], d.get("bias"), d["w13"], d["w2"], k, w.scoring,
-                          w.n_group, w.topk_group, w.renormalize, w.scaling, ws=ws)
+                          w.n_group, w.topk_group, w.renormalize, w.scaling, ws=ws, **lbs)
             lt = []
             for it in range(25):
                 fl.zero_()
@@ -419,12 +448,17 @@ def run_ours(args):
     x_host = d["hidden"].cpu().pin_memory()
     y_host = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
     x_dev = torch.empty_like(d["hidden"])
+    xs_host = d["hidden_scale"].cpu().pin_memory() if w.lowbit else None
+    xs_dev = torch.empty_like(d["hidden_scale"]) if w.lowbit else None
+    lbe = dict(lbk, hidden_scale=xs_dev) if w.lowbit else {}
     y_dev = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
     K2 = max(3, min(K, 50))
     for _ in range(2):
         x_dev.copy_(x_host, non_blocking=True)
+        if w.lowbit:
+            xs_dev.copy_(xs_host, non_blocking=True)
         moe.layer(x_dev, d["gate"], d.get("bias"), d["w13"], d["w2"], k, w.scoring, w.n_group,
-                  w.topk_group, w.renormalize, w.scaling, ws=ws, out=y_dev)
+                  w.topk_group, w.renormalize, w.scaling, ws=ws, out=y_dev, **lbe)
         y_host.copy_(y_dev, non_blocking=True)
     torch.cuda.synchronize()
     barrier(world, dev)
@@ -433,14 +467,17 @@ def run_ours(args):
     a.record(stream)
     for _ in range(K2):
         x_dev.copy_(x_host, non_blocking=True)
+        if w.lowbit:
+            xs_dev.copy_(xs_host, non_blocking=True)
         moe.layer(x_dev, d["gate"], d.get("bias"), d["w13"], d["w2"], k, w.scoring, w.n_group,
-                  w.topk_group, w.renormalize, w.scaling, ws=ws, out=y_dev)
+                  w.topk_group, w.renormalize, w.scaling, ws=ws, out=y_dev, **lbe)
         y_host.copy_(y_dev, non_blocking=True)
     b.record(stream)
     torch.cuda.synchronize()
     e2e_ms = reduce_max(a.elapsed_time(b), world, dev)
+    h2d = x_host.numel() * x_host.element_size() + (xs_host.numel() if w.lowbit else 0)
     e2e = {"value": round(world * T * K2 / (e2e_ms / 1e3), 1), "unit": UNIT,
-           "h2d_bytes_per_step": T * H * 2, "d2h_bytes_per_step": T * H * 2}
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": T * H * 2}
     code = moe.read_device_error(ws.buf)
 
     # ---- CPU oracle baseline (rank 0, N = 1 only) ----
@@ -459,7 +496,9 @@ def run_ours(args):
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3 x e2m1 (f16 MMA, fp32 accumulate)" if w.lowbit else "bf16",
+        "data": "synthetic",
         "config": {"workload": f"{w.name} MoE layer forward (H={H}, E={E}, k={k}, F={F}, "
                                f"{w.scoring}{', groups %d/%d' % (w.n_group, w.topk_group) if w.n_group > 1 else ''}), "
                                f"T={T} tokens, BLOCK_M={BM}, random-init weights",

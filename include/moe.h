@@ -166,9 +166,22 @@ int moe_align(const int32_t* topk_ids, int T, int k, int E, int block_m, int32_t
  * moe_expert_gemm2: stage[a, h] = bf16(weight[a] * sum_f inter[p, f] * w2[e, h, f])
  *   for every real row p (a = sorted_ids[p] < T*k).
  * moe_grouped_ffn: both, with inter held in the workspace.
- * w_dt must equal act_dt (BF16) or be E2M1 with act_dt E4M3 (low-bit:
- * MOE_ERR_UNSUPPORTED until built).  Limits: H % 64 == 0, F % 32 == 0,
- * block_m in {16, 64, 128}.
+ * w_dt must equal act_dt (BF16) or be E2M1 with act_dt E4M3 (low-bit).
+ * Limits: H % 64 == 0, F % 32 == 0 (F % 64 == 0 for low-bit), block_m in
+ * {16, 64, 128} (MOE_ERR_ARG otherwise); any other dtype pair returns
+ * MOE_ERR_UNSUPPORTED.
+ *
+ * Low-bit layouts ([P4] §1.1: FP4 weights, FP8 tokens, one power-of-two
+ * scale byte 2^(s-127) per 32 values along the contraction):
+ *   x [T,H] e4m3 codes, x_scale [T,H/32]; w13 [E,2F,H/2] e2m1 packed (low
+ *   nibble = even column), w13_scale [E,2F,H/32]; inter [cap_rows,F] e4m3
+ *   codes, inter_scale [cap_rows,F/32] (written by gemm1: [P4] §3.5 scale =
+ *   smallest power of two with amax/scale <= 448, codes rounded to nearest
+ *   even and saturated at 448); w2 [E,H,F/2] e2m1, w2_scale [E,H,F/32].
+ *   Products are formed exactly (f16 operands, fp32 accumulation) when every
+ *   scale exponent s-127 lies in [-14, 13] for weights and [-14, 7] for
+ *   activations; exponents outside [-14, 15] are clamped, so such inputs
+ *   give results that differ from the exact dequantised product.
  * ------------------------------------------------------------------------- */
 size_t moe_ffn_workspace_bytes(int T, int H, int F, int E, int k, int block_m, int act_dt);
 int moe_expert_gemm1(const void* x, int act_dt, const uint8_t* x_scale, const void* w13,

@@ -11,8 +11,9 @@
 // epilogue).
 //
 // HBM traffic stays low-bit: converter warps read the packed codes and the
-// scale bytes, dequantise them exactly into f16 (every e2m1 / e4m3 value
-// times 2^u with u in [-14, 15] is an f16 number) in registers, and write the
+// scale bytes, dequantise them into f16 in registers (exact while the value
+// fits: e2m1 x 2^u for u in [-14, 13], e4m3 x 2^u for u in [-14, 7]; the
+// exponent is clamped to [-14, 15] before the multiply), and write the
 // 128-byte-swizzled operand tiles that a single thread feeds to
 // tcgen05.mma kind::f16 (f16 x f16 -> fp32 in TMEM; every product is exact).
 // 16 warps: warp 1 allocates TMEM and issues the MMAs, warps 2-9 convert
