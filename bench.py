@@ -176,6 +176,22 @@ def work_model(w, T, touched, block_m, b_x=None, b_w=None, b_g=None):
     return st, layer
 
 
+class L2Flush:
+    """Evicts the workload from L2 between timed replays: writes a 512 MB
+    buffer (4x L2), then reads a separate 256 MB buffer so the dirty lines of
+    the write are written back before the timed region instead of inside it."""
+
+    def __init__(self, torch, dev):
+        self.w = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+        self.r = torch.zeros((256 << 20) // 4, dtype=torch.int32, device=dev)
+        self.acc = torch.zeros((), dtype=torch.int64, device=dev)
+        self.torch = torch
+
+    def __call__(self):
+        self.w.zero_()
+        self.torch.sum(self.r, (0,), dtype=self.torch.int64, out=self.acc)
+
+
 def roofline_of(bytes_, flops, seconds, peaks):
     t_hbm = bytes_ / (peaks["hbm_gbs"] * 1e9)
     t_tc = flops / (peaks["bf16_tflops"] * 1e12)
@@ -322,9 +338,8 @@ def run_ours(args):
     lbk = dict(hidden_scale=d.get("hidden_scale"), w13_scale=d.get("w13_scale"),
                w2_scale=d.get("w2_scale")) if w.lowbit else {}
     l2_note = ("inputs larger than L2 (expert weights %.2f GB)" % (weights_bytes / 1e9)
-               if weights_bytes > 256e6 else "L2 flushed between steps")
-    flush = None if weights_bytes > 256e6 else torch.empty(512 << 20, dtype=torch.uint8,
-                                                           device=dev)
+               if weights_bytes > 256e6 else "L2 flushed between steps (512 MB write, then 256 MB read)")
+    flush = None if weights_bytes > 256e6 else L2Flush(torch, dev)
 
     def step():
         for n in names:
@@ -332,7 +347,7 @@ def run_ours(args):
 
     for _ in range(args.warmup):
         if flush is not None:
-            flush.zero_()
+            flush()
         step()
     torch.cuda.synchronize()
 
@@ -347,7 +362,7 @@ def run_ours(args):
             t_start.record(stream)
         for i in range(K):
             if flush is not None:
-                flush.zero_()
+                flush()
             for j, n in enumerate(names):
                 ev[i][j].record(stream)
                 graphs[n].replay()
@@ -386,7 +401,7 @@ def run_ours(args):
     # ---- sweep over T: per-kernel times, L2 flushed before each replay ----
     sweep = {}
     if not args.no_sweep and rank == 0:
-        fl = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+        fl = L2Flush(torch, dev)
         for Ts in w.Ts:
             if Ts >= T:
                 continue
@@ -396,7 +411,7 @@ def run_ours(args):
             lbs = dict(lbk, hidden_scale=xsc) if w.lowbit else {}
             times = {n: [] for n in names}
             for it in range(25):
-                fl.zero_()
+                fl()
                 evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)]
                 for j, n in enumerate(names):
                     evs[j].record(stream)
@@ -416,7 +431,7 @@ def run_ours(args):
                           w.n_group, w.topk_group, w.renormalize, w.scaling, ws=ws, **lbs)
             lt = []
             for it in range(25):
-                fl.zero_()
+                fl()
                 e0 = torch.cuda.Event(enable_timing=True)
                 e1 = torch.cuda.Event(enable_timing=True)
                 e0.record(stream)

@@ -91,6 +91,12 @@ static LayerLayout layer_layout(int T, int H, int F, int E, int k, int block_m,
 }
 
 static int* err_word(void* ws) { return reinterpret_cast<int*>(static_cast<char*>(ws) + kWsErrOffset); }
+static int* align_hist(void* ws) {
+  return reinterpret_cast<int*>(static_cast<char*>(ws) + kWsAlignHistOffset);
+}
+static int* align_bar(void* ws) {
+  return reinterpret_cast<int*>(static_cast<char*>(ws) + kWsAlignBarrierOffset);
+}
 
 // ---- checks -------------------------------------------------------------------
 static int check_router(const void* hidden, int hidden_dt, const uint8_t* hidden_scale,
@@ -247,9 +253,10 @@ int moe_align(const int32_t* topk_ids, int T, int k, int E, int block_m, int32_t
     return MOE_ERR_ARG;
   if ((T > 0 && !topk_ids) || !sorted_ids || !block_expert || !num_post_padded || !ws)
     return MOE_ERR_ARG;
-  if (ws_bytes < kWsHeaderBytes) return MOE_ERR_ARG;
+  if (ws_bytes < kWsHeaderBytes || !aligned(ws, 256)) return MOE_ERR_ARG;
   if (launch_align(topk_ids, T, k, E, block_m, sorted_ids, cap_rows, block_expert,
-                   num_post_padded, err_word(ws), static_cast<cudaStream_t>(stream)) != 0)
+                   num_post_padded, align_hist(ws), align_bar(ws), err_word(ws),
+                   static_cast<cudaStream_t>(stream)) != 0)
     return launch_fail("align kernel");
   return MOE_OK;
 }
@@ -459,7 +466,8 @@ int moe_layer(const void* hidden, int act_dt, const uint8_t* hidden_scale, const
                     reinterpret_cast<int*>(base + kWsRouterTicketOffset), err_word(ws), plan,
                     s) != 0)
     return launch_fail("router kernel");
-  if (launch_align(ids, T, k, E, block_m, sorted, L.cap, blk, npp, err_word(ws), s) != 0)
+  if (launch_align(ids, T, k, E, block_m, sorted, L.cap, blk, npp, align_hist(ws), align_bar(ws),
+                   err_word(ws), s) != 0)
     return launch_fail("align kernel");
   const FfnLayout FL = ffn_layout(T, F, E, k, block_m, true, act_dt);
   void* inter = base + L.ffn + FL.inter;

@@ -233,6 +233,42 @@ MOE_DEV int ticket_add_acq_rel(int* p, int v) {
 MOE_DEV void store_relaxed_gpu(int* p, int v) {
   asm volatile("st.relaxed.gpu.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
+MOE_DEV int load_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+MOE_DEV void store_release_gpu(int* p, int v) {
+  asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Barrier over the CTAs of a cooperative launch (all co-resident).  bar[0]
+// counts arrivals and is reset by the last CTA, bar[1] is a generation that
+// the last CTA advances; both start at zero.  The wait is bounded: on expiry
+// it records kErrTimeout and returns (the caller's outputs are then invalid).
+MOE_DEV void grid_barrier(int* bar, int nctas, int* err) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const int gen = load_acquire_gpu(bar + 1);
+    __threadfence();
+    const int old = ticket_add_acq_rel(bar, 1);
+    if (old == nctas - 1) {
+      store_relaxed_gpu(bar, 0);
+      store_release_gpu(bar + 1, gen + 1);
+    } else {
+      const long long t0 = clock64();
+      while (load_acquire_gpu(bar + 1) == gen) {
+        if (clock64() - t0 > kWaitLimitCycles) {
+          raise_error(err, kErrTimeout);
+          break;
+        }
+        __nanosleep(64);
+      }
+    }
+    __threadfence();
+  }
+  __syncthreads();
+}
 
 // Order-preserving map of fp32 onto uint32 (for warp max/min reductions).
 MOE_DEV uint32_t f2ord(float f) {

@@ -15,9 +15,13 @@ namespace moe {
 constexpr size_t kWsErrOffset = 0;                  // int32 sticky error word
 constexpr size_t kWsFfnTicketOffset = 1024;         // int32[kFfnMaxTickets]
 constexpr int kFfnMaxTickets = 1024;
+constexpr size_t kWsAlignBarrierOffset = 5120;      // int32[2] grid barrier of the align kernel
 constexpr size_t kWsRouterTicketOffset = 8192;      // int32[kRouterMaxTiles]
 constexpr int kRouterMaxTiles = 65536;              // token tiles of 16 -> T <= 1,048,576
-constexpr size_t kWsHeaderBytes = kWsRouterTicketOffset + 4ull * kRouterMaxTiles;
+constexpr size_t kWsAlignHistOffset = kWsRouterTicketOffset + 4ull * kRouterMaxTiles;
+constexpr int kAlignMaxCtas = 64;                   // int32[kAlignMaxCtas][kAlignMaxE]
+constexpr int kAlignMaxE = 1024;
+constexpr size_t kWsHeaderBytes = kWsAlignHistOffset + 4ull * kAlignMaxCtas * kAlignMaxE;
 
 constexpr size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -38,9 +42,11 @@ int launch_router(const void* hidden, int hidden_dt, const uint8_t* hidden_scale
                   const RouterPlan& plan, cudaStream_t stream);
 
 // ---- align ------------------------------------------------------------------
+// hist: int32[kAlignMaxCtas * kAlignMaxE] scratch; bar: int32[2], zero before
+// the first call (self-resetting afterwards).
 int launch_align(const int32_t* topk_ids, int T, int k, int E, int block_m, int32_t* sorted_ids,
-                 int64_t cap_rows, int32_t* block_expert, int32_t* num_post_padded, int* err,
-                 cudaStream_t stream);
+                 int64_t cap_rows, int32_t* block_expert, int32_t* num_post_padded, int* hist,
+                 int* bar, int* err, cudaStream_t stream);
 
 // ---- expert GEMMs -------------------------------------------------------------
 struct FfnParams {
