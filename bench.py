@@ -527,7 +527,8 @@ def run_ours(args):
         "stage_us": {n: round(v * 1e3, 2) for n, v in stage_ms.items()},
         "sweep": sweep,
         "e2e": e2e,
-        "gpu_launches": len(names) * K,
+        "gpu_launches": K * (len(names) - 1 + moe.router_kernel_count(
+            T, H, E, "e4m3" if w.lowbit else "bf16", "f32" if w.lowbit else "bf16")),
         "cpu_baseline": cpu,
         "device_error_word": code,
     }

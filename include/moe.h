@@ -83,8 +83,21 @@ typedef enum { MOE_DT_BF16 = 0, MOE_DT_F32 = 1, MOE_DT_E4M3 = 2, MOE_DT_E2M1 = 3
  *   topk_weights [T,k] fp32 out
  * Limits: 1 <= k <= min(E,16), E <= 512, H % 32 == 0.  Logits are fp32 sums
  * of exact products (fp32 inputs are split into three bf16 parts).
+ *
+ * Execution.  Few tokens ([P1] §5.1, the decode regime): one fused launch
+ * whose CTAs split the gate read and whose last CTA per token tile selects.
+ * From 256 tokens, when H % 64 == 0, E % 16 == 0 with E <= 256 (or E % 32 == 0
+ * with E <= 512) and hidden is BF16 or E4M3: the gate GEMM runs on the tensor
+ * cores in 128-token tiles with the K range split over CTAs, and a second
+ * launch sums each token's split partials in split order and selects (plus
+ * one conversion launch first when hidden is E4M3 or the gate is F32).  Both
+ * paths give the same ids except where two rank keys are within fp32
+ * summation-order noise of each other.
+ * moe_router_kernel_count returns how many kernels moe_router enqueues for
+ * these shapes and types (0 when T == 0).
  * ------------------------------------------------------------------------- */
 size_t moe_router_workspace_bytes(int T, int H, int E);
+int moe_router_kernel_count(int T, int H, int E, int hidden_dt, int gate_dt);
 int moe_router(const void* hidden, int hidden_dt, const uint8_t* hidden_scale, const void* gate,
                int gate_dt, const float* bias, int T, int H, int E, int k, int scoring,
                int n_group, int topk_group, int renormalize, float scaling, int32_t* topk_ids,
@@ -103,7 +116,9 @@ int moe_router(const void* hidden, int hidden_dt, const uint8_t* hidden_scale, c
  * so the caller passes only the inputs and the outputs, exactly as for
  * moe_router, and nothing is allocated or freed.
  *
- *   - Same arguments, rules and results as moe_router, without ws/ws_bytes.
+ *   - Same arguments and rules as moe_router, without ws/ws_bytes; always
+ *     the one-launch kernel, so its ids can differ from moe_router's tiled
+ *     path only on near-ties (see Execution above).
  *   - Limit: the partial logits of one call, KS * T * E * 4 bytes with the
  *     K-split count KS the router picks (16 for a few tokens, 1 for thousands),
  *     must fit in MOE_ROUTER_NOALLOC_MAX_LOGIT_BYTES (8 MiB), and
@@ -167,9 +182,9 @@ int moe_align(const int32_t* topk_ids, int T, int k, int E, int block_m, int32_t
  *   for every real row p (a = sorted_ids[p] < T*k).
  * moe_grouped_ffn: both, with inter held in the workspace.
  * w_dt must equal act_dt (BF16) or be E2M1 with act_dt E4M3 (low-bit).
- * Limits: H % 64 == 0, F % 32 == 0 (F % 64 == 0 for low-bit), block_m in
- * {16, 64, 128} (MOE_ERR_ARG otherwise); any other dtype pair returns
- * MOE_ERR_UNSUPPORTED.
+ * Limits: H % 64 == 0, F % 32 == 0 (low-bit: H % 128 == 0, F % 128 == 0 and
+ * every scale array 4-byte aligned), block_m in {16, 64, 128} (MOE_ERR_ARG
+ * otherwise); any other dtype pair returns MOE_ERR_UNSUPPORTED.
  *
  * Low-bit layouts ([P4] §1.1: FP4 weights, FP8 tokens, one power-of-two
  * scale byte 2^(s-127) per 32 values along the contraction):

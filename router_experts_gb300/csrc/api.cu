@@ -139,7 +139,9 @@ static int check_ffn(int act_dt, int w_dt, int T, int H, int F, int E, int k, in
     return MOE_ERR_ARG;
   if (act_dt == MOE_DT_BF16 && w_dt == MOE_DT_BF16) return MOE_OK;
   if (act_dt == MOE_DT_E4M3 && w_dt == MOE_DT_E2M1)
-    return (F % 64 == 0) ? MOE_OK : MOE_ERR_ARG;  // both contractions in whole 64-steps
+    // both contractions in whole 128-value steps: every scale row is a whole
+    // number of 4-byte words
+    return (F % 128 == 0 && H % 128 == 0) ? MOE_OK : MOE_ERR_ARG;
   return MOE_ERR_UNSUPPORTED;
 }
 
@@ -219,6 +221,13 @@ size_t moe_router_workspace_bytes(int T, int H, int E) {
   return kWsHeaderBytes + plan_router(T, H, E).scratch_bytes;
 }
 
+int moe_router_kernel_count(int T, int H, int E, int hidden_dt, int gate_dt) {
+  if (T <= 0 || H <= 0 || E <= 0) return 0;
+  const RouterPlan p = plan_router(T, H, E);
+  if (!router_uses_tiled(p, hidden_dt, gate_dt)) return 1;
+  return 2 + ((hidden_dt == MOE_DT_E4M3 || gate_dt == MOE_DT_F32) ? 1 : 0);
+}
+
 int moe_router(const void* hidden, int hidden_dt, const uint8_t* hidden_scale, const void* gate,
                int gate_dt, const float* bias, int T, int H, int E, int k, int scoring,
                int n_group, int topk_group, int renormalize, float scaling, int32_t* topk_ids,
@@ -280,8 +289,9 @@ static int expert_gemm_lowbit(int kind, const void* act, const uint8_t* act_scal
     return MOE_ERR_ARG;
   if (kind == 0 && (!inter_q || !inter_scale)) return MOE_ERR_ARG;
   if (kind == 1 && (!topk_weights || !stage)) return MOE_ERR_ARG;
-  if (!aligned(act, 16) || !aligned(w, 16) || !aligned(w_scale, 2) ||
-      (inter_q && !aligned(inter_q, 32)) || (stage && !aligned(stage, 32)))
+  if (!aligned(act, 16) || !aligned(w, 16) || !aligned(act_scale, 4) || !aligned(w_scale, 4) ||
+      (inter_q && !aligned(inter_q, 32)) || (inter_scale && !aligned(inter_scale, 4)) ||
+      (stage && !aligned(stage, 32)))
     return MOE_ERR_ARG;
   LowbitParams p{};
   p.sorted_ids = sorted_ids;

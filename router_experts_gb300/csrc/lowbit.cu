@@ -32,12 +32,20 @@ namespace moe {
 namespace {
 
 constexpr int kLbThreads = 512;
-constexpr int kLbStages = 4;
+constexpr int kLbStages = 2;                // f16 operand stages
 constexpr int kLbA = 128 * 128;             // 128 token rows x 64 f16
 constexpr int kLbB = 256 * 128;             // 256 weight rows x 64 f16
 constexpr int kLbStage = kLbA + kLbB;       // 48 KB
 constexpr int kLbConv = 256;                // converter threads (warps 2-9)
-constexpr int kLbSmem = kLbStages * kLbStage + 1024 + 512;
+// Raw codes are staged per converter thread: each K step's 32 weight-code
+// bytes, 32 token-code bytes and the aligned words holding their scale bytes
+// land in the thread's own shared-memory slot by cp.async, kLbDepth steps
+// ahead of their conversion.
+constexpr int kLbDepth = 6;
+constexpr int kLbSlot = 80;                 // 32 W | 32 X | 4 W scales | 4 X scale | pad
+constexpr int kLbRawBytes = kLbDepth * kLbConv * kLbSlot;
+constexpr int kLbSmem = kLbStages * kLbStage + kLbRawBytes + 1024 + 512;
+static_assert(kLbSmem <= 232448, "shared memory budget");
 constexpr uint32_t kLbIdesc = (1u << 4) | (static_cast<uint32_t>(256 >> 3) << 17) |
                               (static_cast<uint32_t>(128 >> 4) << 24);  // f16 x f16 -> f32
 
@@ -86,19 +94,19 @@ struct LbUnit {
   int b, n, e;
 };
 
-// The raw bytes one converter thread reads for one K step.
-struct LbRaw {
-  uint4 w0, w1;     // 64 e2m1 codes of the weight row
-  uint32_t wsc;     // its two scale bytes (low = first 32)
-  uint4 t0, t1;     // 32 e4m3 codes of half a token row
-  uint32_t tsc;     // its scale byte
-  bool wvalid, tvalid;
+// Source rows of one converter thread for one unit: weight row ct of the
+// tile and half (ct & 1) of token row ct >> 1.  Null pointers stand for
+// padding (their copies zero-fill the slot).
+struct LbRows {
+  const uint8_t* w;    // weight codes of the row (K/2 bytes)
+  const uint8_t* wsc;  // its scale bytes (K/32)
+  const uint8_t* x;    // token codes of the row (K bytes)
+  const uint8_t* xsc;  // its scale bytes (K/32)
 };
 
 template <int KIND>
-MOE_DEV void lb_load(const LowbitParams& p, const LbUnit& u, int kb, int ct, int K,
-                     LbRaw& r) {
-  // weight row ct of the tile
+MOE_DEV LbRows lb_rows(const LowbitParams& p, const LbUnit& u, int ct, int K) {
+  LbRows r{};
   int wrow;
   bool wv;
   if constexpr (KIND == 0) {
@@ -110,69 +118,89 @@ MOE_DEV void lb_load(const LowbitParams& p, const LbUnit& u, int kb, int ct, int
     wv = hr < p.H;
     wrow = u.e * p.H + hr;
   }
-  r.wvalid = wv;
   if (wv) {
-    const uint4* src = reinterpret_cast<const uint4*>(
-        p.w + static_cast<size_t>(wrow) * (K / 2) + static_cast<size_t>(kb) * 32);
-    r.w0 = __ldg(src);
-    r.w1 = __ldg(src + 1);
-    r.wsc = __ldg(reinterpret_cast<const uint16_t*>(
-        p.w_scale + static_cast<size_t>(wrow) * (K / 32) + static_cast<size_t>(kb) * 2));
+    r.w = p.w + static_cast<size_t>(wrow) * (K / 2);
+    r.wsc = p.w_scale + static_cast<size_t>(wrow) * (K / 32);
   }
-  // half (ct & 1) of token row ct >> 1
-  const int tr = ct >> 1, half = ct & 1;
-  r.tvalid = false;
+  const int tr = ct >> 1;
   if (tr < p.BM) {
     const size_t prow = static_cast<size_t>(u.b) * p.BM + tr;
-    const uint8_t* base = nullptr;
-    const uint8_t* sbase = nullptr;
     if constexpr (KIND == 0) {
       const int a = __ldg(p.sorted_ids + prow);
       if (a >= 0 && a < p.T * p.k) {
         const size_t tok = static_cast<size_t>(a / p.k);
-        base = p.act + tok * K;
-        sbase = p.act_scale + tok * (K / 32);
+        r.x = p.act + tok * K;
+        r.xsc = p.act_scale + tok * (K / 32);
       }
     } else {
-      base = p.act + prow * K;
-      sbase = p.act_scale + prow * (K / 32);
-    }
-    if (base) {
-      const uint4* src =
-          reinterpret_cast<const uint4*>(base + static_cast<size_t>(kb) * 64 + half * 32);
-      r.t0 = __ldg(src);
-      r.t1 = __ldg(src + 1);
-      r.tsc = __ldg(sbase + static_cast<size_t>(kb) * 2 + half);
-      r.tvalid = true;
+      r.x = p.act + prow * K;
+      r.xsc = p.act_scale + prow * (K / 32);
     }
   }
+  return r;
 }
 
-// Dequantise one K step into the swizzled f16 operand tiles of a stage.
-MOE_DEV void lb_store(const LbRaw& r, int ct, int BM, uint32_t a_tile, uint32_t b_tile) {
+// cp.async of K step kb into a slot: 32 weight-code bytes, the 32 token-code
+// bytes of this thread's half row, and the 4-byte words holding the scale
+// bytes (every scale row starts 4-byte aligned and spans a multiple of 4
+// bytes, so a word never leaves its row).
+MOE_DEV void lb_issue(const LbRows& r, int kb, int half, uint32_t slot, const void* dummy) {
+  const uint8_t* w = r.w ? r.w + static_cast<size_t>(kb) * 32 : nullptr;
+  const uint8_t* x = r.x ? r.x + static_cast<size_t>(kb) * 64 + half * 32 : nullptr;
+  cp_async_16(slot, w ? static_cast<const void*>(w) : dummy, w ? 16u : 0u);
+  cp_async_16(slot + 16, w ? static_cast<const void*>(w + 16) : dummy, w ? 16u : 0u);
+  cp_async_16(slot + 32, x ? static_cast<const void*>(x) : dummy, x ? 16u : 0u);
+  cp_async_16(slot + 48, x ? static_cast<const void*>(x + 16) : dummy, x ? 16u : 0u);
+  cp_async_4(slot + 64, r.wsc ? static_cast<const void*>(r.wsc + ((2 * kb) & ~3)) : dummy,
+             r.wsc ? 4u : 0u);
+  cp_async_4(slot + 68, r.xsc ? static_cast<const void*>(r.xsc + ((2 * kb + half) & ~3)) : dummy,
+             r.xsc ? 4u : 0u);
+}
+
+MOE_DEV uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
+MOE_DEV uint32_t ld_shared_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+
+// Dequantise K step kb from a slot into the swizzled f16 operand tiles: the
+// weight row ct into B, and (rows present in the block) half a token row into
+// A.  Zero-filled codes of padding give zeros whatever their scale.
+MOE_DEV void lb_convert(uint32_t slot, int kb, int ct, int BM, uint32_t a_tile, uint32_t b_tile) {
+  const uint4 w0 = ld_shared_v4(slot), w1 = ld_shared_v4(slot + 16);
+  const uint32_t wsw = ld_shared_u32(slot + 64);
   {
+    const int b0 = (2 * kb) & 3;
+    const uint32_t s_lo = scale_f16x2((wsw >> (8 * b0)) & 0xFFu);
+    const uint32_t s_hi = scale_f16x2((wsw >> (8 * (b0 + 1))) & 0xFFu);
+    const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
     const uint32_t row = ct;
-    const uint32_t s_lo = scale_f16x2(r.wsc & 0xFFu), s_hi = scale_f16x2((r.wsc >> 8) & 0xFFu);
-    const uint32_t words[8] = {r.w0.x, r.w0.y, r.w0.z, r.w0.w, r.w1.x, r.w1.y, r.w1.z, r.w1.w};
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      uint32_t o[4] = {0u, 0u, 0u, 0u};
-      if (r.wvalid) fp4x8_to_f16(words[j], j < 4 ? s_lo : s_hi, o);
-      const uint32_t dst = b_tile + row * 128 + ((j ^ (row & 7)) << 4);
-      st_shared_v4(dst, o);
+      uint32_t o[4];
+      fp4x8_to_f16(words[j], j < 4 ? s_lo : s_hi, o);
+      st_shared_v4(b_tile + row * 128 + ((j ^ (row & 7)) << 4), o);
     }
   }
   const int tr = ct >> 1, half = ct & 1;
   if (tr < BM) {
-    const uint32_t s2 = scale_f16x2(r.tsc);
-    const uint32_t words[8] = {r.t0.x, r.t0.y, r.t0.z, r.t0.w, r.t1.x, r.t1.y, r.t1.z, r.t1.w};
+    const uint4 x0 = ld_shared_v4(slot + 32), x1 = ld_shared_v4(slot + 48);
+    const uint32_t xsw = ld_shared_u32(slot + 68);
+    const uint32_t s2 = scale_f16x2((xsw >> (8 * ((2 * kb + half) & 3))) & 0xFFu);
+    const uint32_t words[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      uint32_t o[4] = {0u, 0u, 0u, 0u};
-      if (r.tvalid) fp8x8_to_f16(words[2 * j], words[2 * j + 1], s2, o);
+      uint32_t o[4];
+      fp8x8_to_f16(words[2 * j], words[2 * j + 1], s2, o);
       const int chunk = half * 4 + j;
-      const uint32_t dst = a_tile + tr * 128 + ((chunk ^ (tr & 7)) << 4);
-      st_shared_v4(dst, o);
+      st_shared_v4(a_tile + tr * 128 + ((chunk ^ (tr & 7)) << 4), o);
     }
   }
 }
@@ -210,7 +238,7 @@ __global__ void __launch_bounds__(kLbThreads, 1) lowbit_gemm_kernel(const Lowbit
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + kLbStages * kLbStage);
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + kLbStages * kLbStage + kLbRawBytes);
   uint64_t* empty_bar = full_bar + kLbStages;
   uint64_t* tfull_bar = empty_bar + kLbStages;
   uint64_t* tempty_bar = tfull_bar + 2;
@@ -228,7 +256,7 @@ __global__ void __launch_bounds__(kLbThreads, 1) lowbit_gemm_kernel(const Lowbit
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kLbStages; ++i) {
-      mbar_init(&full_bar[i], kLbConv);
+      mbar_init(&full_bar[i], kLbConv / 32);  // one arrival per converter warp
       mbar_init(&empty_bar[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -290,28 +318,52 @@ __global__ void __launch_bounds__(kLbThreads, 1) lowbit_gemm_kernel(const Lowbit
     }
   } else if (warp >= 2 && warp < 10) {
     // ---------------- converters ----------------
+    // Each thread runs its own cp.async pipeline kLbDepth K steps deep over
+    // the flat sequence (unit, K step) of this CTA; it reads back only its own
+    // slots, so cp.async.wait_group alone orders copy and use.
     const int ct = threadIdx.x - 64;  // 0..255
+    const int half = ct & 1;
+    const uint32_t raw0 = smem_u32(smem + kLbStages * kLbStage) + ct * kLbSlot;
+    constexpr uint32_t kRawStride = kLbConv * kLbSlot;
+    int iu = blockIdx.x, ikb = 0;
+    LbRows ir{};
+    if (iu < num_units) ir = lb_rows<KIND>(p, decode(iu), ct, K);
+    uint32_t q_issue = 0;
+    auto issue_next = [&]() {
+      if (iu < num_units) {
+        lb_issue(ir, ikb, half, raw0 + (q_issue % kLbDepth) * kRawStride, p.w);
+        if (++ikb == KB) {
+          ikb = 0;
+          iu += gridDim.x;
+          if (iu < num_units) ir = lb_rows<KIND>(p, decode(iu), ct, K);
+        }
+      }
+      cp_async_commit();  // empty groups past the end keep the group count uniform
+      ++q_issue;
+    };
+    for (int d = 0; d < kLbDepth - 1; ++d) issue_next();
     uint32_t it = 0;
     bool alive = true;
     for (int uu = blockIdx.x; alive && uu < num_units; uu += gridDim.x) {
-      const LbUnit u = decode(uu);
-      LbRaw cur, nxt;
-      lb_load<KIND>(p, u, 0, ct, K, cur);
       for (int kb = 0; kb < KB; ++kb, ++it) {
-        if (kb + 1 < KB) lb_load<KIND>(p, u, kb + 1, ct, K, nxt);
+        issue_next();
+        cp_async_wait<kLbDepth - 1>();  // this thread's copies of step `it` have landed
         const int st = it % kLbStages;
         const uint32_t ph = (it / kLbStages) & 1u;
-        if (!mbar_wait(&empty_bar[st], ph ^ 1u, abort_flag, p.err)) {
+        // the warp stops as one (its lanes meet at __syncwarp below)
+        const bool ok = mbar_wait(&empty_bar[st], ph ^ 1u, abort_flag, p.err);
+        if (__any_sync(0xffffffffu, !ok)) {
           alive = false;
           break;
         }
         const uint32_t a_tile = smem_u32(smem + st * kLbStage);
-        lb_store(cur, ct, p.BM, a_tile, a_tile + kLbA);
+        lb_convert(raw0 + (it % kLbDepth) * kRawStride, kb, ct, p.BM, a_tile, a_tile + kLbA);
         fence_proxy_async_smem();  // generic-proxy tile writes -> tensor core reads
-        mbar_arrive(&full_bar[st]);
-        cur = nxt;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&full_bar[st]);
       }
     }
+    cp_async_wait_all();
   } else if (warp >= 12) {
     // ---------------- epilogue ----------------
     const int ew = warp - 12;

@@ -108,6 +108,11 @@ MOE_DEV void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes) {
                "r"(src_bytes)
                : "memory");
 }
+MOE_DEV void cp_async_4(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
 MOE_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 // Arrive on `bar` (counted in its expected arrivals) once all cp.async copies
 // issued so far by this thread have landed; the thread does not wait.

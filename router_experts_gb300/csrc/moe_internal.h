@@ -27,14 +27,23 @@ constexpr size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 // ---- router -----------------------------------------------------------------
 struct RouterPlan {
+  // fused one-launch kernel (any T)
   int nb8;        // n8 tiles of experts per CTA (1 or 8)
   int et;         // experts per CTA
   int ne;         // expert tiles
   int nt;         // token tiles of 16
   int ks;         // K splits across CTAs
+  // tiled tensor-core path (many tokens; bf16 or e4m3 hidden, bf16 or fp32 gate)
+  bool tiled;
+  int tnt;        // token tiles of 128
+  int tks;        // K splits across CTAs
+  size_t xb_off, gp_off;  // offsets in the scratch of the bf16 x and the gate planes
   size_t scratch_bytes;
 };
-RouterPlan plan_router(int T, int H, int E);
+// allow_tiled = false keeps every T on the fused kernel.
+RouterPlan plan_router(int T, int H, int E, bool allow_tiled = true);
+// hidden_dt: 0 bf16, 1 f32, 2 e4m3; gate_dt: 0 bf16, 1 f32
+bool router_uses_tiled(const RouterPlan& plan, int hidden_dt, int gate_dt);
 int launch_router(const void* hidden, int hidden_dt, const uint8_t* hidden_scale,
                   const void* gate, int gate_dt, const float* bias, int T, int H, int E, int k,
                   int scoring, int n_group, int topk_group, int renormalize, float scaling,
@@ -93,5 +102,10 @@ int launch_lowbit_gemm(int kind, const LowbitParams& p, int num_sms, cudaStream_
 int launch_finalize(const void* stage, int T, int k, int H, void* out, cudaStream_t stream);
 
 int device_num_sms();
+
+// 2-D bf16 tensor map of a row-major [rows, cols] matrix: 128-byte swizzle,
+// box = 64 columns x box_rows rows, zero fill out of bounds.
+bool make_map_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
+                   uint32_t box_rows);
 
 }  // namespace moe

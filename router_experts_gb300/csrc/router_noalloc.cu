@@ -75,7 +75,7 @@ extern "C" int moe_router_noalloc(const void* hidden, int hidden_dt, const uint8
   if (!aligned16(hidden) || !aligned16(gate)) return MOE_ERR_ARG;
 
   // the static array bounds the problem size
-  const moe::RouterPlan plan = moe::plan_router(T, H, E);
+  const moe::RouterPlan plan = moe::plan_router(T, H, E, false);
   if (plan.nt > kMaxTokenTiles || plan.scratch_bytes > kLogitBytes) return MOE_ERR_ARG;
 
   void* base = nullptr;

@@ -9,11 +9,15 @@ shapes in between, and check that oversized problems are refused.  The file is
 collected last on purpose."""
 import ctypes
 
+import numpy as np
 import pytest
 import torch
 
+import oracle
 from router_experts_gb300 import moe
 from router_experts_gb300 import workloads as W
+
+from _gpu import GAP_MIN, oracle_router
 
 pytestmark = pytest.mark.gpu
 
@@ -64,8 +68,16 @@ def test_noalloc_matches_router_on_consecutive_calls(seq):
         ref_ids, ref_w = reference(w, d)
         ids, wts = call_noalloc(fn, w, d, T)
         torch.cuda.synchronize()
-        assert torch.equal(ids, ref_ids), name
-        assert (wts - ref_w).abs().max().item() <= WEIGHT_ATOL
+        # moe_router may take its tiled tensor-core path for many tokens, which
+        # sums the logits in another order: ids may differ only on tokens that
+        # the oracle shows to be near-ties at the cut
+        same = (ids == ref_ids).all(dim=1).cpu().numpy()
+        diff = np.nonzero(~same)[0].astype(np.int32)
+        assert diff.size <= max(2, T // 100), (name, diff.size)
+        if diff.size:
+            _, _, gap = oracle_router(oracle, w, d, T, diff)
+            assert (gap <= GAP_MIN).all(), (name, diff[gap > GAP_MIN])
+        assert (wts - ref_w).abs()[torch.as_tensor(same, device=wts.device)].max().item() <= WEIGHT_ATOL
 
 
 def test_noalloc_rejects_sizes_beyond_its_array():
