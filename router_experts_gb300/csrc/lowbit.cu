@@ -64,24 +64,40 @@ MOE_DEV uint32_t hmul2_u32(uint32_t a, uint32_t b) {
 }
 
 // 4 bytes = 8 e2m1 codes (low nibble first) -> 8 f16 (4 registers), scaled.
+// One hardware conversion per byte (two codes; the low nibble becomes the low
+// half of the f16 pair), then one f16x2 multiply by the power-of-two scale.
 MOE_DEV void fp4x8_to_f16(uint32_t w, uint32_t s2, uint32_t (&o)[4]) {
+  uint32_t h[4];
+  asm("{\n"
+      " .reg .b8 q0, q1, q2, q3;\n"
+      " mov.b32 {q0, q1, q2, q3}, %4;\n"
+      " cvt.rn.f16x2.e2m1x2 %0, q0;\n"
+      " cvt.rn.f16x2.e2m1x2 %1, q1;\n"
+      " cvt.rn.f16x2.e2m1x2 %2, q2;\n"
+      " cvt.rn.f16x2.e2m1x2 %3, q3;\n"
+      "}"
+      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+      : "r"(w));
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const __nv_fp4x2_storage_t b = static_cast<__nv_fp4x2_storage_t>((w >> (8 * i)) & 0xFFu);
-    __half2_raw h = __nv_cvt_fp4x2_to_halfraw2(b, __NV_E2M1);
-    o[i] = hmul2_u32(*reinterpret_cast<uint32_t*>(&h), s2);
-  }
+  for (int i = 0; i < 4; ++i) o[i] = hmul2_u32(h[i], s2);
 }
-// 8 bytes = 8 e4m3 codes -> 8 f16 (4 registers), scaled.
+// 8 bytes = 8 e4m3 codes -> 8 f16 (4 registers), scaled: one hardware
+// conversion per code pair (low byte -> low half), one f16x2 multiply.
 MOE_DEV void fp8x8_to_f16(uint32_t lo, uint32_t hi, uint32_t s2, uint32_t (&o)[4]) {
-  const uint32_t w[2] = {lo, hi};
+  uint32_t h[4];
+  asm("{\n"
+      " .reg .b16 p0, p1, p2, p3;\n"
+      " mov.b32 {p0, p1}, %4;\n"
+      " mov.b32 {p2, p3}, %5;\n"
+      " cvt.rn.f16x2.e4m3x2 %0, p0;\n"
+      " cvt.rn.f16x2.e4m3x2 %1, p1;\n"
+      " cvt.rn.f16x2.e4m3x2 %2, p2;\n"
+      " cvt.rn.f16x2.e4m3x2 %3, p3;\n"
+      "}"
+      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+      : "r"(lo), "r"(hi));
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const __nv_fp8x2_storage_t b =
-        static_cast<__nv_fp8x2_storage_t>((w[i / 2] >> (16 * (i % 2))) & 0xFFFFu);
-    __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(b, __NV_E4M3);
-    o[i] = hmul2_u32(*reinterpret_cast<uint32_t*>(&h), s2);
-  }
+  for (int i = 0; i < 4; ++i) o[i] = hmul2_u32(h[i], s2);
 }
 
 MOE_DEV void st_shared_v4(uint32_t addr, const uint32_t (&v)[4]) {
