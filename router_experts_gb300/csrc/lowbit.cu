@@ -10,18 +10,30 @@
 // sorted_ids, gather folded into the load, weight in the down GEMM's
 // epilogue).
 //
-// HBM traffic stays low-bit: converter warps read the packed codes and the
-// scale bytes, dequantise them into f16 in registers (exact while the value
-// fits: e2m1 x 2^u for u in [-14, 13], e4m3 x 2^u for u in [-14, 7]; the
-// exponent is clamped to [-14, 15] before the multiply), and write the
-// 128-byte-swizzled operand tiles that a single thread feeds to
-// tcgen05.mma kind::f16 (f16 x f16 -> fp32 in TMEM; every product is exact).
-// 16 warps: warp 1 allocates TMEM and issues the MMAs, warps 2-9 convert
-// (one weight row and half a token row each per stage), warps 12-15 run the
-// epilogue; the others idle.  Tile: M = 128 token rows of one block (BLOCK_M
-// rows valid), N = 256 weight rows, K steps of 64, four stages, two
-// double-buffered 256-column accumulators.
-#include <cuda_fp4.h>
+// The products run on the block-scaled tensor-core MMA
+// (tcgen05.mma kind::mxf8f6f4 with one UE8M0 scale per 32 values of each
+// operand row, fp32 accumulation in TMEM), so the scales are applied by the
+// tensor core and the operands stay one byte wide in shared memory:
+//   A = 128 token rows of e4m3 codes, gathered as they are (no conversion);
+//   B = 128 weight rows, e2m1 codes widened to e4m3 (exact: every e2m1 value
+//       is an e4m3 value) by converter warps;
+//   scale factors are written to TMEM with tcgen05.st: for row m of A, lane m
+//   and column base + m/32; for row n of B, lane n mod 32 (in every lane
+//   quarter) and column base + n/32; byte j of the word scales the j-th
+//   32-value block of a 128-value K step.
+// Tile: M = 128 token rows of one block (BLOCK_M rows valid), N = 128 weight
+// rows (GEMM1: 64 gate rows + the matching 64 up rows), K steps of 128 (four
+// K=32 MMAs).  Two 128-column accumulators, double-buffered.
+// 16 warps:
+//   warp 0      TMA of the packed weight codes (ring of 8 raw stages) and,
+//               one row per lane, cp.async of their scale words
+//   warp 1      TMEM allocation and the single thread issuing the MMAs
+//   warps 2-3   cp.async gather of the token codes and scale words straight
+//               into the operand stage (ring of 4)
+//   warps 4-11  widen the weight codes into the operand stage; warps 4-7
+//               write the token scale factors to TMEM, warps 8-11 the weight
+//               scale factors
+//   warps 12-15 epilogue (TMEM lane quarter = warp % 4)
 #include <cuda_fp8.h>
 
 #include "moe_common.cuh"
@@ -31,42 +43,59 @@ namespace moe {
 
 namespace {
 
-constexpr int kLbThreads = 512;
-constexpr int kLbStages = 2;                // f16 operand stages
-constexpr int kLbA = 128 * 128;             // 128 token rows x 64 f16
-constexpr int kLbB = 256 * 128;             // 256 weight rows x 64 f16
-constexpr int kLbStage = kLbA + kLbB;       // 48 KB
-constexpr int kLbConv = 256;                // converter threads (warps 2-9)
-// Raw codes are staged per converter thread: each K step's 32 weight-code
-// bytes, 32 token-code bytes and the aligned words holding their scale bytes
-// land in the thread's own shared-memory slot by cp.async, kLbDepth steps
-// ahead of their conversion.
-constexpr int kLbDepth = 6;
-constexpr int kLbSlot = 80;                 // 32 W | 32 X | 4 W scales | 4 X scale | pad
-constexpr int kLbRawBytes = kLbDepth * kLbConv * kLbSlot;
-constexpr int kLbSmem = kLbStages * kLbStage + kLbRawBytes + 1024 + 512;
-static_assert(kLbSmem <= 232448, "shared memory budget");
-constexpr uint32_t kLbIdesc = (1u << 4) | (static_cast<uint32_t>(256 >> 3) << 17) |
-                              (static_cast<uint32_t>(128 >> 4) << 24);  // f16 x f16 -> f32
+constexpr int kMxThreads = 512;
+constexpr int kMxBK = 128;                  // K values per stage (4 MMAs of K = 32)
+constexpr int kMxNT = 128;                  // weight rows per tile (MMA N)
+constexpr int kMxOpStages = 4;              // operand stages (A + B tiles, scale factors)
+constexpr int kMxRawStages = 8;             // raw weight-code stages
+constexpr int kMxA = 128 * kMxBK;           // 16 KB of token codes
+constexpr int kMxB = kMxNT * kMxBK;         // 16 KB of widened weight codes
+constexpr int kMxOp = kMxA + kMxB;
+constexpr int kMxRawW = kMxNT * (kMxBK / 2);  // 8 KB of packed weight codes
+constexpr int kMxOpBytes = kMxOpStages * kMxOp;
+constexpr int kMxRawBytes = kMxRawStages * kMxRawW;
+constexpr int kMxSfaBytes = kMxOpStages * 128 * 4;   // token scale words per op stage
+constexpr int kMxSfbBytes = kMxRawStages * kMxNT * 4;  // weight scale words per raw stage
+constexpr int kMxBarBytes = 512;
+constexpr int kMxSmem = kMxOpBytes + kMxRawBytes + kMxSfaBytes + kMxSfbBytes + kMxBarBytes + 1024;
+static_assert(kMxSmem <= 232448, "shared memory budget");
+constexpr uint32_t kMxAccCols = 128;        // per accumulator buffer
+constexpr uint32_t kMxSfCol0 = 256;         // scale-factor columns: 8 per op stage
+constexpr uint32_t kMxTmemCols = 512;
 
-// f16x2 holding 2^(code-127) twice (exponent clamped to the normal f16 range).
-MOE_DEV uint32_t scale_f16x2(uint32_t code) {
-  int e = static_cast<int>(code) - 127;
-  e = max(-14, min(15, e));
-  const uint32_t h = static_cast<uint32_t>(e + 15) << 10;
-  return h | (h << 16);
+// Instruction descriptor of the block-scaled MMA: e4m3 A and B (K-major),
+// UE8M0 scales, fp32 D; sf_id picks the scale byte of the 32-bit TMEM word.
+__host__ __device__ constexpr uint32_t idesc_mxf8(int M, int N, int sf_id) {
+  return (static_cast<uint32_t>(sf_id) << 4) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (1u << 23) | (static_cast<uint32_t>(M >> 4) << 24) | (static_cast<uint32_t>(sf_id) << 29);
 }
 
-MOE_DEV uint32_t hmul2_u32(uint32_t a, uint32_t b) {
-  __half2 x = *reinterpret_cast<__half2*>(&a), y = *reinterpret_cast<__half2*>(&b);
-  __half2 r = __hmul2(x, y);
-  return *reinterpret_cast<uint32_t*>(&r);
+// D[tmem] (+)= (A * sa)[smem] * (B * sb)[smem]^T with per-32 UE8M0 scales in TMEM.
+MOE_DEV void umma_mxf8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                       uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, "
+      "[%4], [%5], p;\n}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
 }
 
-// 4 bytes = 8 e2m1 codes (low nibble first) -> 8 f16 (4 registers), scaled.
-// One hardware conversion per byte (two codes; the low nibble becomes the low
-// half of the f16 pair), then one f16x2 multiply by the power-of-two scale.
-MOE_DEV void fp4x8_to_f16(uint32_t w, uint32_t s2, uint32_t (&o)[4]) {
+// Warp-wide TMEM stores (lane i of the warp -> TMEM lane (address lane field + i)).
+MOE_DEV void tmem_st1(uint32_t taddr, uint32_t v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
+}
+MOE_DEV void tmem_st4(uint32_t taddr, uint32_t v0, uint32_t v1, uint32_t v2, uint32_t v3) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr),
+               "r"(v0), "r"(v1), "r"(v2), "r"(v3)
+               : "memory");
+}
+MOE_DEV void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// 4 bytes = 8 e2m1 codes (low nibble first) -> 8 e4m3 codes (two words, in
+// order): hardware e2m1x2 -> f16x2 and f16x2 -> e4m3x2 conversions, both
+// exact on these values.
+MOE_DEV uint2 e2m1x8_to_e4m3x8(uint32_t w) {
   uint32_t h[4];
   asm("{\n"
       " .reg .b8 q0, q1, q2, q3;\n"
@@ -78,101 +107,21 @@ MOE_DEV void fp4x8_to_f16(uint32_t w, uint32_t s2, uint32_t (&o)[4]) {
       "}"
       : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
       : "r"(w));
+  uint32_t o[4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) o[i] = hmul2_u32(h[i], s2);
-}
-// 8 bytes = 8 e4m3 codes -> 8 f16 (4 registers), scaled: one hardware
-// conversion per code pair (low byte -> low half), one f16x2 multiply.
-MOE_DEV void fp8x8_to_f16(uint32_t lo, uint32_t hi, uint32_t s2, uint32_t (&o)[4]) {
-  uint32_t h[4];
-  asm("{\n"
-      " .reg .b16 p0, p1, p2, p3;\n"
-      " mov.b32 {p0, p1}, %4;\n"
-      " mov.b32 {p2, p3}, %5;\n"
-      " cvt.rn.f16x2.e4m3x2 %0, p0;\n"
-      " cvt.rn.f16x2.e4m3x2 %1, p1;\n"
-      " cvt.rn.f16x2.e4m3x2 %2, p2;\n"
-      " cvt.rn.f16x2.e4m3x2 %3, p3;\n"
-      "}"
-      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
-      : "r"(lo), "r"(hi));
-#pragma unroll
-  for (int i = 0; i < 4; ++i) o[i] = hmul2_u32(h[i], s2);
+  for (int i = 0; i < 4; ++i) {
+    uint16_t b;
+    asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(b) : "r"(h[i]));
+    o[i] = b;
+  }
+  return make_uint2(o[0] | (o[1] << 16), o[2] | (o[3] << 16));
 }
 
-MOE_DEV void st_shared_v4(uint32_t addr, const uint32_t (&v)[4]) {
-  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v[0]), "r"(v[1]),
-               "r"(v[2]), "r"(v[3])
+MOE_DEV void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
                : "memory");
 }
-
-struct LbUnit {
-  int b, n, e;
-};
-
-// Source rows of one converter thread for one unit: weight row ct of the
-// tile and half (ct & 1) of token row ct >> 1.  Null pointers stand for
-// padding (their copies zero-fill the slot).
-struct LbRows {
-  const uint8_t* w;    // weight codes of the row (K/2 bytes)
-  const uint8_t* wsc;  // its scale bytes (K/32)
-  const uint8_t* x;    // token codes of the row (K bytes)
-  const uint8_t* xsc;  // its scale bytes (K/32)
-};
-
-template <int KIND>
-MOE_DEV LbRows lb_rows(const LowbitParams& p, const LbUnit& u, int ct, int K) {
-  LbRows r{};
-  int wrow;
-  bool wv;
-  if constexpr (KIND == 0) {
-    const int fr = u.n * 128 + (ct & 127);
-    wv = fr < p.F;
-    wrow = u.e * 2 * p.F + ((ct < 128) ? 0 : p.F) + fr;
-  } else {
-    const int hr = u.n * 256 + ct;
-    wv = hr < p.H;
-    wrow = u.e * p.H + hr;
-  }
-  if (wv) {
-    r.w = p.w + static_cast<size_t>(wrow) * (K / 2);
-    r.wsc = p.w_scale + static_cast<size_t>(wrow) * (K / 32);
-  }
-  const int tr = ct >> 1;
-  if (tr < p.BM) {
-    const size_t prow = static_cast<size_t>(u.b) * p.BM + tr;
-    if constexpr (KIND == 0) {
-      const int a = __ldg(p.sorted_ids + prow);
-      if (a >= 0 && a < p.T * p.k) {
-        const size_t tok = static_cast<size_t>(a / p.k);
-        r.x = p.act + tok * K;
-        r.xsc = p.act_scale + tok * (K / 32);
-      }
-    } else {
-      r.x = p.act + prow * K;
-      r.xsc = p.act_scale + prow * (K / 32);
-    }
-  }
-  return r;
-}
-
-// cp.async of K step kb into a slot: 32 weight-code bytes, the 32 token-code
-// bytes of this thread's half row, and the 4-byte words holding the scale
-// bytes (every scale row starts 4-byte aligned and spans a multiple of 4
-// bytes, so a word never leaves its row).
-MOE_DEV void lb_issue(const LbRows& r, int kb, int half, uint32_t slot, const void* dummy) {
-  const uint8_t* w = r.w ? r.w + static_cast<size_t>(kb) * 32 : nullptr;
-  const uint8_t* x = r.x ? r.x + static_cast<size_t>(kb) * 64 + half * 32 : nullptr;
-  cp_async_16(slot, w ? static_cast<const void*>(w) : dummy, w ? 16u : 0u);
-  cp_async_16(slot + 16, w ? static_cast<const void*>(w + 16) : dummy, w ? 16u : 0u);
-  cp_async_16(slot + 32, x ? static_cast<const void*>(x) : dummy, x ? 16u : 0u);
-  cp_async_16(slot + 48, x ? static_cast<const void*>(x + 16) : dummy, x ? 16u : 0u);
-  cp_async_4(slot + 64, r.wsc ? static_cast<const void*>(r.wsc + ((2 * kb) & ~3)) : dummy,
-             r.wsc ? 4u : 0u);
-  cp_async_4(slot + 68, r.xsc ? static_cast<const void*>(r.xsc + ((2 * kb + half) & ~3)) : dummy,
-             r.xsc ? 4u : 0u);
-}
-
 MOE_DEV uint4 ld_shared_v4(uint32_t addr) {
   uint4 v;
   asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
@@ -184,41 +133,6 @@ MOE_DEV uint32_t ld_shared_u32(uint32_t addr) {
   uint32_t v;
   asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
   return v;
-}
-
-// Dequantise K step kb from a slot into the swizzled f16 operand tiles: the
-// weight row ct into B, and (rows present in the block) half a token row into
-// A.  Zero-filled codes of padding give zeros whatever their scale.
-MOE_DEV void lb_convert(uint32_t slot, int kb, int ct, int BM, uint32_t a_tile, uint32_t b_tile) {
-  const uint4 w0 = ld_shared_v4(slot), w1 = ld_shared_v4(slot + 16);
-  const uint32_t wsw = ld_shared_u32(slot + 64);
-  {
-    const int b0 = (2 * kb) & 3;
-    const uint32_t s_lo = scale_f16x2((wsw >> (8 * b0)) & 0xFFu);
-    const uint32_t s_hi = scale_f16x2((wsw >> (8 * (b0 + 1))) & 0xFFu);
-    const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-    const uint32_t row = ct;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      uint32_t o[4];
-      fp4x8_to_f16(words[j], j < 4 ? s_lo : s_hi, o);
-      st_shared_v4(b_tile + row * 128 + ((j ^ (row & 7)) << 4), o);
-    }
-  }
-  const int tr = ct >> 1, half = ct & 1;
-  if (tr < BM) {
-    const uint4 x0 = ld_shared_v4(slot + 32), x1 = ld_shared_v4(slot + 48);
-    const uint32_t xsw = ld_shared_u32(slot + 68);
-    const uint32_t s2 = scale_f16x2((xsw >> (8 * ((2 * kb + half) & 3))) & 0xFFu);
-    const uint32_t words[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      uint32_t o[4];
-      fp8x8_to_f16(words[2 * j], words[2 * j + 1], s2, o);
-      const int chunk = half * 4 + j;
-      st_shared_v4(a_tile + tr * 128 + ((chunk ^ (tr & 7)) << 4), o);
-    }
-  }
 }
 
 // e4m3 codes of 32 activations with their UE8M0 exponent byte: scale = the
@@ -249,47 +163,76 @@ MOE_DEV uint32_t requant32(const float (&v)[32], uint32_t (&codes)[8]) {
   return static_cast<uint32_t>(s + 127);
 }
 
+struct MxUnit {
+  int b, n, e;
+};
+
+// Weight row r (0..127) of the tile of unit u: GEMM1 gate rows n*64 + r for
+// r < 64 and the matching up rows for r >= 64; GEMM2 rows n*128 + r.
 template <int KIND>
-__global__ void __launch_bounds__(kLbThreads, 1) lowbit_gemm_kernel(const LowbitParams p) {
+MOE_DEV int mx_wrow(const LowbitParams& p, const MxUnit& u, int r) {
+  if constexpr (KIND == 0) {
+    const int f = u.n * (kMxNT / 2) + (r & 63);
+    return u.e * 2 * p.F + ((r < 64) ? 0 : p.F) + f;
+  } else {
+    return u.e * p.H + u.n * kMxNT + r;
+  }
+}
+
+template <int KIND>
+__global__ void __launch_bounds__(kMxThreads, 1)
+    lowbit_gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const LowbitParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + kLbStages * kLbStage + kLbRawBytes);
-  uint64_t* empty_bar = full_bar + kLbStages;
-  uint64_t* tfull_bar = empty_bar + kLbStages;
-  uint64_t* tempty_bar = tfull_bar + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty_bar + 2);
+  uint8_t* op = smem;                 // [kMxOpStages][A tile | B tile]
+  uint8_t* raw = op + kMxOpBytes;     // [kMxRawStages][128 rows x 64 bytes]
+  uint32_t* sfa = reinterpret_cast<uint32_t*>(raw + kMxRawBytes);  // [kMxOpStages][128]
+  uint32_t* sfb = sfa + kMxOpStages * 128;                         // [kMxRawStages][128]
+  uint64_t* wfull = reinterpret_cast<uint64_t*>(sfb + kMxRawStages * kMxNT);
+  uint64_t* wempty = wfull + kMxRawStages;
+  uint64_t* afull = wempty + kMxRawStages;
+  uint64_t* ready = afull + kMxOpStages;
+  uint64_t* oempty = ready + kMxOpStages;
+  uint64_t* tfull = oempty + kMxOpStages;
+  uint64_t* tempty = tfull + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int K = (KIND == 0) ? p.H : p.F;
-  const int KB = K / 64;
+  const int KS = K / kMxBK;
   int npp = __ldg(p.num_post_padded);
   npp = max(0, min(npp, p.cap_rows));
   const int nblk = npp / p.BM;
-  const int ntiles = (KIND == 0) ? (p.F + 127) / 128 : (p.H + 255) / 256;
+  const int ntiles = (KIND == 0) ? p.F / (kMxNT / 2) : p.H / kMxNT;
   const int num_units = nblk * ntiles;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kLbStages; ++i) {
-      mbar_init(&full_bar[i], kLbConv / 32);  // one arrival per converter warp
-      mbar_init(&empty_bar[i], 1);
+    for (int i = 0; i < kMxRawStages; ++i) {
+      mbar_init(&wfull[i], 1 + 32);  // TMA bytes + the scale-word copies of warp 0
+      mbar_init(&wempty[i], 8);      // converter warps
+    }
+    for (int i = 0; i < kMxOpStages; ++i) {
+      mbar_init(&afull[i], 64);      // gather threads
+      mbar_init(&ready[i], 8);       // converter warps
+      mbar_init(&oempty[i], 1);      // MMA commit
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&tfull_bar[i], 1);
-      mbar_init(&tempty_bar[i], 4);
+      mbar_init(&tfull[i], 1);
+      mbar_init(&tempty[i], 4);
     }
     *abort_flag = 0;
     mbar_fence_init();
   }
-  if (warp == 1) tmem_alloc(tmem_slot, 512);
+  if (warp == 1) tmem_alloc(tmem_slot, kMxTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
   auto decode = [&](int uu) {
-    LbUnit u;
+    MxUnit u;
     u.b = uu / ntiles;
     u.n = uu % ntiles;
     int e = __ldg(p.block_expert + u.b);
@@ -301,7 +244,40 @@ __global__ void __launch_bounds__(kLbThreads, 1) lowbit_gemm_kernel(const Lowbit
     return u;
   };
 
-  if (warp == 1) {
+  if (warp == 0) {
+    // ---------------- packed weight codes (TMA) + their scale words ----------------
+    if (lane == 0) tma_prefetch_desc(&tm_w);
+    uint32_t it = 0;
+    bool alive = true;
+    for (int uu = blockIdx.x; alive && uu < num_units; uu += gridDim.x) {
+      const MxUnit u = decode(uu);
+      const uint8_t* srow[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        srow[i] = p.w_scale + static_cast<size_t>(mx_wrow<KIND>(p, u, lane + 32 * i)) * (K / 32);
+      const int r0 = mx_wrow<KIND>(p, u, 0), r64 = mx_wrow<KIND>(p, u, 64);
+      for (int ks = 0; ks < KS; ++ks, ++it) {
+        const int ws = it % kMxRawStages;
+        const uint32_t ph = (it / kMxRawStages) & 1u;
+        const bool ok = mbar_wait(&wempty[ws], ph ^ 1u, abort_flag, p.err);
+        if (__any_sync(0xffffffffu, !ok)) {
+          alive = false;
+          break;
+        }
+        if (lane == 0) {
+          uint8_t* dst = raw + ws * kMxRawW;
+          mbar_arrive_expect_tx(&wfull[ws], kMxRawW);
+          tma_load_2d(dst, &tm_w, &wfull[ws], ks * (kMxBK / 2), r0);
+          tma_load_2d(dst + 64 * 64, &tm_w, &wfull[ws], ks * (kMxBK / 2), r64);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          cp_async_4(smem_u32(sfb + ws * kMxNT + lane + 32 * i), srow[i] + ks * 4, 4u);
+        cp_async_mbar_arrive_noinc(&wfull[ws]);
+      }
+    }
+    cp_async_wait_all();
+  } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
       uint32_t it = 0, acc_it = 0;
@@ -309,101 +285,169 @@ __global__ void __launch_bounds__(kLbThreads, 1) lowbit_gemm_kernel(const Lowbit
       for (int uu = blockIdx.x; alive && uu < num_units; uu += gridDim.x, ++acc_it) {
         const int buf = acc_it & 1;
         const uint32_t aph = (acc_it >> 1) & 1u;
-        if (!mbar_wait(&tempty_bar[buf], aph ^ 1u, abort_flag, p.err)) break;
+        if (!mbar_wait(&tempty[buf], aph ^ 1u, abort_flag, p.err)) break;
         tc_fence_after();
-        const uint32_t d = tmem_base + buf * 256;
-        for (int kb = 0; kb < KB; ++kb, ++it) {
-          const int st = it % kLbStages;
-          const uint32_t ph = (it / kLbStages) & 1u;
-          if (!mbar_wait(&full_bar[st], ph, abort_flag, p.err)) {
+        const uint32_t d = tmem_base + buf * kMxAccCols;
+        for (int ks = 0; ks < KS; ++ks, ++it) {
+          const int s = it % kMxOpStages;
+          const uint32_t ph = (it / kMxOpStages) & 1u;
+          if (!mbar_wait(&ready[s], ph, abort_flag, p.err)) {
             alive = false;
             break;
           }
+          fence_proxy_async_smem();  // cp.async token rows -> tensor core
           tc_fence_after();
-          const uint32_t a_addr = smem_u32(smem + st * kLbStage);
-          const uint32_t b_addr = a_addr + kLbA;
+          const uint32_t a_addr = smem_u32(op + s * kMxOp);
+          const uint32_t b_addr = a_addr + kMxA;
+          const uint32_t sfa_t = tmem_base + kMxSfCol0 + 8 * s;
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            umma_f16(d, sw128_desc(a_addr + kk * 32), sw128_desc(b_addr + kk * 32), kLbIdesc,
-                     (kb > 0 || kk > 0) ? 1u : 0u);
-          umma_commit(&empty_bar[st]);
+          for (int kk = 0; kk < kMxBK / 32; ++kk)
+            umma_mxf8(d, sw128_desc(a_addr + kk * 32), sw128_desc(b_addr + kk * 32),
+                      idesc_mxf8(128, kMxNT, kk), sfa_t, sfa_t + 4, (ks > 0 || kk > 0) ? 1u : 0u);
+          umma_commit(&oempty[s]);
         }
         if (!alive) break;
-        umma_commit(&tfull_bar[buf]);
+        umma_commit(&tfull[buf]);
       }
     }
-  } else if (warp >= 2 && warp < 10) {
-    // ---------------- converters ----------------
-    // Each thread runs its own cp.async pipeline kLbDepth K steps deep over
-    // the flat sequence (unit, K step) of this CTA; it reads back only its own
-    // slots, so cp.async.wait_group alone orders copy and use.
-    const int ct = threadIdx.x - 64;  // 0..255
-    const int half = ct & 1;
-    const uint32_t raw0 = smem_u32(smem + kLbStages * kLbStage) + ct * kLbSlot;
-    constexpr uint32_t kRawStride = kLbConv * kLbSlot;
-    int iu = blockIdx.x, ikb = 0;
-    LbRows ir{};
-    if (iu < num_units) ir = lb_rows<KIND>(p, decode(iu), ct, K);
-    uint32_t q_issue = 0;
-    auto issue_next = [&]() {
-      if (iu < num_units) {
-        lb_issue(ir, ikb, half, raw0 + (q_issue % kLbDepth) * kRawStride, p.w);
-        if (++ikb == KB) {
-          ikb = 0;
-          iu += gridDim.x;
-          if (iu < num_units) ir = lb_rows<KIND>(p, decode(iu), ct, K);
-        }
+  } else if (warp < 4) {
+    // ---------------- token codes + scale words (cp.async gather) ----------------
+    const int gt = threadIdx.x - 64;  // 0..63
+    const int chunk = gt & 7;
+    uint32_t it = 0;
+    bool alive = true;
+    auto row_src = [&](const MxUnit& u, int r, const uint8_t*& codes, const uint8_t*& scales) {
+      codes = nullptr;
+      scales = nullptr;
+      if (r >= p.BM) return;
+      const size_t prow = static_cast<size_t>(u.b) * p.BM + r;
+      if constexpr (KIND == 0) {
+        const int a = __ldg(p.sorted_ids + prow);
+        if (a < 0 || a >= p.T * p.k) return;
+        const size_t tok = static_cast<size_t>(a / p.k);
+        codes = p.act + tok * K;
+        scales = p.act_scale + tok * (K / 32);
+      } else {
+        codes = p.act + prow * K;
+        scales = p.act_scale + prow * (K / 32);
       }
-      cp_async_commit();  // empty groups past the end keep the group count uniform
-      ++q_issue;
     };
-    for (int d = 0; d < kLbDepth - 1; ++d) issue_next();
+    for (int uu = blockIdx.x; alive && uu < num_units; uu += gridDim.x) {
+      const MxUnit u = decode(uu);
+      const uint8_t* src[16];
+      const uint8_t* ssrc[2];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const uint8_t* sc;
+        row_src(u, (gt >> 3) + 8 * i, src[i], sc);
+      }
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const uint8_t* cd;
+        row_src(u, gt + 64 * j, cd, ssrc[j]);
+      }
+      for (int ks = 0; ks < KS; ++ks, ++it) {
+        const int s = it % kMxOpStages;
+        const uint32_t ph = (it / kMxOpStages) & 1u;
+        if (!mbar_wait(&oempty[s], ph ^ 1u, abort_flag, p.err)) {
+          alive = false;
+          break;
+        }
+        const uint32_t tile = smem_u32(op + s * kMxOp);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int r = (gt >> 3) + 8 * i;
+          const uint32_t dst = tile + r * 128 + ((chunk ^ (r & 7)) << 4);
+          cp_async_16(dst, src[i] ? static_cast<const void*>(src[i] + ks * kMxBK + chunk * 16) : p.act,
+                      src[i] ? 16u : 0u);
+        }
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+          cp_async_4(smem_u32(sfa + s * 128 + gt + 64 * j),
+                     ssrc[j] ? static_cast<const void*>(ssrc[j] + ks * 4) : p.act_scale,
+                     ssrc[j] ? 4u : 0u);
+        // the stage barrier counts this thread's arrival when its copies land
+        cp_async_mbar_arrive_noinc(&afull[s]);
+      }
+    }
+    cp_async_wait_all();
+  } else if (warp < 12) {
+    // ---------------- weight codes -> e4m3 operand, scale factors -> TMEM ----------------
+    const int ct = threadIdx.x - 128;  // 0..255: half (ct & 1) of weight row ct >> 1
+    const int row = ct >> 1, half = ct & 1;
+    const int q = warp & 3;            // this warp's TMEM lane quarter
+    const bool token_sf = warp < 8;    // warps 4-7: token scales, warps 8-11: weight scales
+    const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
     uint32_t it = 0;
     bool alive = true;
     for (int uu = blockIdx.x; alive && uu < num_units; uu += gridDim.x) {
-      for (int kb = 0; kb < KB; ++kb, ++it) {
-        issue_next();
-        cp_async_wait<kLbDepth - 1>();  // this thread's copies of step `it` have landed
-        const int st = it % kLbStages;
-        const uint32_t ph = (it / kLbStages) & 1u;
-        // the warp stops as one (its lanes meet at __syncwarp below)
-        const bool ok = mbar_wait(&empty_bar[st], ph ^ 1u, abort_flag, p.err);
+      for (int ks = 0; ks < KS; ++ks, ++it) {
+        const int s = it % kMxOpStages, ws = it % kMxRawStages;
+        const uint32_t ph = (it / kMxOpStages) & 1u, wph = (it / kMxRawStages) & 1u;
+        bool ok = mbar_wait(&oempty[s], ph ^ 1u, abort_flag, p.err);
+        ok = ok && mbar_wait(&wfull[ws], wph, abort_flag, p.err);
+        if (token_sf) ok = ok && mbar_wait(&afull[s], ph, abort_flag, p.err);
+        // the warp stops as one (its lanes meet in the warp-wide TMEM stores)
         if (__any_sync(0xffffffffu, !ok)) {
           alive = false;
           break;
         }
-        const uint32_t a_tile = smem_u32(smem + st * kLbStage);
-        lb_convert(raw0 + (it % kLbDepth) * kRawStride, kb, ct, p.BM, a_tile, a_tile + kLbA);
+        // 32 packed bytes (64 codes) of the row -> 64 e4m3 bytes, 128-byte swizzle
+        const uint32_t rsrc = smem_u32(raw + ws * kMxRawW) + row * 64 + half * 32;
+        const uint4 w0 = ld_shared_v4(rsrc), w1 = ld_shared_v4(rsrc + 16);
+        const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+        const uint32_t bt = smem_u32(op + s * kMxOp + kMxA) + row * 128;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint2 lo = e2m1x8_to_e4m3x8(words[2 * j]);
+          const uint2 hi = e2m1x8_to_e4m3x8(words[2 * j + 1]);
+          const int c = 4 * half + j;
+          st_shared_v4(bt + ((c ^ (row & 7)) << 4), lo.x, lo.y, hi.x, hi.y);
+        }
+        const uint32_t sf_col = kMxSfCol0 + 8 * s;
+        if (token_sf) {
+          // token row 32q + lane: lane 32q + lane, column sf_col + q
+          tmem_st1(lane_base + sf_col + q,
+                   ld_shared_u32(smem_u32(sfa + s * 128 + q * 32 + lane)));
+        } else {
+          // weight row 32c + lane: lane (mod 32) of every quarter, column sf_col + 4 + c
+          const uint32_t* w = sfb + ws * kMxNT;
+          tmem_st4(lane_base + sf_col + 4, w[lane], w[32 + lane], w[64 + lane], w[96 + lane]);
+        }
+        tmem_st_wait();
         fence_proxy_async_smem();  // generic-proxy tile writes -> tensor core reads
+        tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&full_bar[st]);
+        if (lane == 0) {
+          mbar_arrive(&ready[s]);
+          mbar_arrive(&wempty[ws]);
+        }
       }
     }
-    cp_async_wait_all();
   } else if (warp >= 12) {
     // ---------------- epilogue ----------------
-    const int ew = warp - 12;
+    const int ew = warp & 3;
     const int row = ew * 32 + lane;
     uint32_t acc_it = 0;
     for (int uu = blockIdx.x; uu < num_units; uu += gridDim.x, ++acc_it) {
-      const LbUnit u = decode(uu);
+      const MxUnit u = decode(uu);
       const int buf = acc_it & 1;
       const uint32_t aph = (acc_it >> 1) & 1u;
-      const bool ok = mbar_wait(&tfull_bar[buf], aph, abort_flag, p.err);
+      const bool ok = mbar_wait(&tfull[buf], aph, abort_flag, p.err);
       if (named_bar_any(1, 128, !ok || *abort_flag)) break;
       tc_fence_after();
-      const uint32_t tb = tmem_base + (static_cast<uint32_t>(ew * 32) << 16) + buf * 256;
+      const uint32_t tb = tmem_base + (static_cast<uint32_t>(ew * 32) << 16) + buf * kMxAccCols;
       const bool rvalid = row < p.BM;
       const size_t prow = static_cast<size_t>(u.b) * p.BM + row;
       if constexpr (KIND == 0) {
-        // SwiGLU of gate column c and up column 128 + c, re-quantised per 32
+        // SwiGLU of gate column c and up column 64 + c, re-quantised per 32
 #pragma unroll 1
-        for (int j = 0; j < 4; ++j) {
+        for (int j = 0; j < 2; ++j) {
           uint32_t g0[16], g1[16], u0[16], u1[16];
           tmem_ld16(tb + 32 * j, g0);
           tmem_ld16(tb + 32 * j + 16, g1);
-          tmem_ld16(tb + 128 + 32 * j, u0);
-          tmem_ld16(tb + 128 + 32 * j + 16, u1);
+          tmem_ld16(tb + 64 + 32 * j, u0);
+          tmem_ld16(tb + 64 + 32 * j + 16, u1);
           tmem_ld_wait();
           reg_fence16(g0);
           reg_fence16(g1);
@@ -417,7 +461,7 @@ __global__ void __launch_bounds__(kLbThreads, 1) lowbit_gemm_kernel(const Lowbit
           }
           uint32_t codes[8];
           const uint32_t sbyte = requant32(act, codes);
-          const int f = u.n * 128 + 32 * j;
+          const int f = u.n * (kMxNT / 2) + 32 * j;
           if (rvalid && f + 32 <= p.F) {
             st_global_v8(p.inter_q + prow * p.F + f, codes);
             p.inter_scale[prow * (p.F / 32) + f / 32] = static_cast<uint8_t>(sbyte);
@@ -429,12 +473,12 @@ __global__ void __launch_bounds__(kLbThreads, 1) lowbit_gemm_kernel(const Lowbit
         const bool valid = rvalid && a >= 0 && a < p.T * p.k;
         const float w = valid ? __ldg(p.topk_weights + a) : 0.f;
 #pragma unroll 1
-        for (int c = 0; c < 16; ++c) {
+        for (int c = 0; c < kMxNT / 16; ++c) {
           uint32_t r[16];
           tmem_ld16(tb + 16 * c, r);
           tmem_ld_wait();
           reg_fence16(r);
-          const int h = u.n * 256 + 16 * c;
+          const int h = u.n * kMxNT + 16 * c;
           if (valid && h + 16 <= p.H) {
             uint32_t o[8];
 #pragma unroll
@@ -446,14 +490,14 @@ __global__ void __launch_bounds__(kLbThreads, 1) lowbit_gemm_kernel(const Lowbit
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty_bar[buf]);
+      if (lane == 0) mbar_arrive(&tempty[buf]);
     }
   }
 
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, 512);
+    tmem_dealloc(tmem_base, kMxTmemCols);
   }
 }
 
@@ -463,16 +507,22 @@ int launch_lowbit_gemm(int kind, const LowbitParams& p, int num_sms, cudaStream_
   static bool attr_set = false;
   if (!attr_set) {
     if (cudaFuncSetAttribute(lowbit_gemm_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kLbSmem) != cudaSuccess ||
+                             kMxSmem) != cudaSuccess ||
         cudaFuncSetAttribute(lowbit_gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kLbSmem) != cudaSuccess)
+                             kMxSmem) != cudaSuccess)
       return -1;
     attr_set = true;
   }
+  // packed weight codes [E*2F or E*H rows, K/2 bytes], box 64 bytes x 64 rows
+  const int K = (kind == 0) ? p.H : p.F;
+  const uint64_t rows = (kind == 0) ? static_cast<uint64_t>(p.E) * 2 * p.F
+                                    : static_cast<uint64_t>(p.E) * p.H;
+  CUtensorMap tm_w;
+  if (!make_map_u8(&tm_w, p.w, rows, static_cast<uint64_t>(K) / 2, 64, 64)) return -1;
   if (kind == 0)
-    lowbit_gemm_kernel<0><<<num_sms, kLbThreads, kLbSmem, stream>>>(p);
+    lowbit_gemm_kernel<0><<<num_sms, kMxThreads, kMxSmem, stream>>>(tm_w, p);
   else
-    lowbit_gemm_kernel<1><<<num_sms, kLbThreads, kLbSmem, stream>>>(p);
+    lowbit_gemm_kernel<1><<<num_sms, kMxThreads, kMxSmem, stream>>>(tm_w, p);
   return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 

@@ -107,5 +107,9 @@ int device_num_sms();
 // box = 64 columns x box_rows rows, zero fill out of bounds.
 bool make_map_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
                    uint32_t box_rows);
+// 2-D byte tensor map of a row-major [rows, cols] byte matrix, no swizzle,
+// box = box_cols bytes x box_rows rows, zero fill out of bounds.
+bool make_map_u8(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
+                 uint32_t box_cols, uint32_t box_rows);
 
 }  // namespace moe
