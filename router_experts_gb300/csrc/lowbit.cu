@@ -25,12 +25,13 @@
 // rows (GEMM1: 64 gate rows + the matching 64 up rows), K steps of 128 (four
 // K=32 MMAs).  Two 128-column accumulators, double-buffered.
 // 16 warps:
-//   warp 0      TMA of the packed weight codes (ring of 8 raw stages) and,
+//   warp 0      TMA of the packed weight codes (ring of 6 raw stages, L2
+//               warmed one ring ahead) and,
 //               one row per lane, cp.async of their scale words
 //   warp 1      TMEM allocation and the single thread issuing the MMAs
 //   warps 2-3   cp.async gather of the token codes and scale words straight
-//               into the operand stage (ring of 4)
-//   warps 4-11  widen the weight codes into the operand stage; warps 4-7
+//               into the token-tile ring (6 deep: it covers the gather latency)
+//   warps 4-11  widen the weight codes into the weight-tile ring (4 deep); warps 4-7
 //               write the token scale factors to TMEM, warps 8-11 the weight
 //               scale factors
 //   warps 12-15 epilogue (TMEM lane quarter = warp % 4)
@@ -46,21 +47,25 @@ namespace {
 constexpr int kMxThreads = 512;
 constexpr int kMxBK = 128;                  // K values per stage (4 MMAs of K = 32)
 constexpr int kMxNT = 128;                  // weight rows per tile (MMA N)
-constexpr int kMxOpStages = 4;              // operand stages (A + B tiles, scale factors)
-constexpr int kMxRawStages = 8;             // raw weight-code stages
+// Token tiles wait on gather latency, so their ring is deep; the widened
+// weight tiles are written just ahead of their MMAs, so theirs is short.
+constexpr int kMxAStages = 6;               // token-code tiles
+constexpr int kMxBStages = 4;               // widened weight tiles (and scale-factor slots)
+constexpr int kMxRawStages = 6;             // packed weight-code stages (streamed from HBM)
 constexpr int kMxA = 128 * kMxBK;           // 16 KB of token codes
 constexpr int kMxB = kMxNT * kMxBK;         // 16 KB of widened weight codes
-constexpr int kMxOp = kMxA + kMxB;
 constexpr int kMxRawW = kMxNT * (kMxBK / 2);  // 8 KB of packed weight codes
-constexpr int kMxOpBytes = kMxOpStages * kMxOp;
+constexpr int kMxABytes = kMxAStages * kMxA;
+constexpr int kMxBBytes = kMxBStages * kMxB;
 constexpr int kMxRawBytes = kMxRawStages * kMxRawW;
-constexpr int kMxSfaBytes = kMxOpStages * 128 * 4;   // token scale words per op stage
+constexpr int kMxSfaBytes = kMxAStages * 128 * 4;      // token scale words per token tile
 constexpr int kMxSfbBytes = kMxRawStages * kMxNT * 4;  // weight scale words per raw stage
 constexpr int kMxBarBytes = 512;
-constexpr int kMxSmem = kMxOpBytes + kMxRawBytes + kMxSfaBytes + kMxSfbBytes + kMxBarBytes + 1024;
+constexpr int kMxSmem =
+    kMxABytes + kMxBBytes + kMxRawBytes + kMxSfaBytes + kMxSfbBytes + kMxBarBytes + 1024;
 static_assert(kMxSmem <= 232448, "shared memory budget");
 constexpr uint32_t kMxAccCols = 128;        // per accumulator buffer
-constexpr uint32_t kMxSfCol0 = 256;         // scale-factor columns: 8 per op stage
+constexpr uint32_t kMxSfCol0 = 256;         // scale-factor columns: 8 per weight-tile slot
 constexpr uint32_t kMxTmemCols = 512;
 
 // Instruction descriptor of the block-scaled MMA: e4m3 A and B (K-major),
@@ -185,16 +190,18 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  uint8_t* op = smem;                 // [kMxOpStages][A tile | B tile]
-  uint8_t* raw = op + kMxOpBytes;     // [kMxRawStages][128 rows x 64 bytes]
-  uint32_t* sfa = reinterpret_cast<uint32_t*>(raw + kMxRawBytes);  // [kMxOpStages][128]
-  uint32_t* sfb = sfa + kMxOpStages * 128;                         // [kMxRawStages][128]
+  uint8_t* atile = smem;                  // [kMxAStages][128 token rows x 128 codes]
+  uint8_t* btile = atile + kMxABytes;     // [kMxBStages][128 weight rows x 128 codes]
+  uint8_t* raw = btile + kMxBBytes;       // [kMxRawStages][128 rows x 64 bytes]
+  uint32_t* sfa = reinterpret_cast<uint32_t*>(raw + kMxRawBytes);  // [kMxAStages][128]
+  uint32_t* sfb = sfa + kMxAStages * 128;                          // [kMxRawStages][128]
   uint64_t* wfull = reinterpret_cast<uint64_t*>(sfb + kMxRawStages * kMxNT);
   uint64_t* wempty = wfull + kMxRawStages;
   uint64_t* afull = wempty + kMxRawStages;
-  uint64_t* ready = afull + kMxOpStages;
-  uint64_t* oempty = ready + kMxOpStages;
-  uint64_t* tfull = oempty + kMxOpStages;
+  uint64_t* aempty = afull + kMxAStages;
+  uint64_t* ready = aempty + kMxAStages;
+  uint64_t* bempty = ready + kMxBStages;
+  uint64_t* tfull = bempty + kMxBStages;
   uint64_t* tempty = tfull + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -213,10 +220,13 @@ __global__ void __launch_bounds__(kMxThreads, 1)
       mbar_init(&wfull[i], 1 + 32);  // TMA bytes + the scale-word copies of warp 0
       mbar_init(&wempty[i], 8);      // converter warps
     }
-    for (int i = 0; i < kMxOpStages; ++i) {
+    for (int i = 0; i < kMxAStages; ++i) {
       mbar_init(&afull[i], 64);      // gather threads
+      mbar_init(&aempty[i], 1);      // MMA commit
+    }
+    for (int i = 0; i < kMxBStages; ++i) {
       mbar_init(&ready[i], 8);       // converter warps
-      mbar_init(&oempty[i], 1);      // MMA commit
+      mbar_init(&bempty[i], 1);      // MMA commit
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&tfull[i], 1);
@@ -256,7 +266,23 @@ __global__ void __launch_bounds__(kMxThreads, 1)
       for (int i = 0; i < 4; ++i)
         srow[i] = p.w_scale + static_cast<size_t>(mx_wrow<KIND>(p, u, lane + 32 * i)) * (K / 32);
       const int r0 = mx_wrow<KIND>(p, u, 0), r64 = mx_wrow<KIND>(p, u, 64);
+      // the next unit of this CTA, for warming L2 one raw ring ahead
+      const bool has_next = uu + static_cast<int>(gridDim.x) < num_units;
+      const MxUnit nu = has_next ? decode(uu + gridDim.x) : u;
+      const int n0 = mx_wrow<KIND>(p, nu, 0), n64 = mx_wrow<KIND>(p, nu, 64);
       for (int ks = 0; ks < KS; ++ks, ++it) {
+        if (lane == 0) {
+          int pk = ks + kMxRawStages, p0 = r0, p64 = r64;
+          if (pk >= KS && has_next) {
+            pk -= KS;
+            p0 = n0;
+            p64 = n64;
+          }
+          if (pk < KS) {
+            tma_prefetch_l2_2d(&tm_w, pk * (kMxBK / 2), p0);
+            tma_prefetch_l2_2d(&tm_w, pk * (kMxBK / 2), p64);
+          }
+        }
         const int ws = it % kMxRawStages;
         const uint32_t ph = (it / kMxRawStages) & 1u;
         const bool ok = mbar_wait(&wempty[ws], ph ^ 1u, abort_flag, p.err);
@@ -289,22 +315,24 @@ __global__ void __launch_bounds__(kMxThreads, 1)
         tc_fence_after();
         const uint32_t d = tmem_base + buf * kMxAccCols;
         for (int ks = 0; ks < KS; ++ks, ++it) {
-          const int s = it % kMxOpStages;
-          const uint32_t ph = (it / kMxOpStages) & 1u;
-          if (!mbar_wait(&ready[s], ph, abort_flag, p.err)) {
+          const int sa = it % kMxAStages, sb = it % kMxBStages;
+          const uint32_t bph = (it / kMxBStages) & 1u;
+          // the converters signal after the token tile of this step has landed
+          if (!mbar_wait(&ready[sb], bph, abort_flag, p.err)) {
             alive = false;
             break;
           }
           fence_proxy_async_smem();  // cp.async token rows -> tensor core
           tc_fence_after();
-          const uint32_t a_addr = smem_u32(op + s * kMxOp);
-          const uint32_t b_addr = a_addr + kMxA;
-          const uint32_t sfa_t = tmem_base + kMxSfCol0 + 8 * s;
+          const uint32_t a_addr = smem_u32(atile + sa * kMxA);
+          const uint32_t b_addr = smem_u32(btile + sb * kMxB);
+          const uint32_t sfa_t = tmem_base + kMxSfCol0 + 8 * sb;
 #pragma unroll
           for (int kk = 0; kk < kMxBK / 32; ++kk)
             umma_mxf8(d, sw128_desc(a_addr + kk * 32), sw128_desc(b_addr + kk * 32),
                       idesc_mxf8(128, kMxNT, kk), sfa_t, sfa_t + 4, (ks > 0 || kk > 0) ? 1u : 0u);
-          umma_commit(&oempty[s]);
+          umma_commit(&aempty[sa]);
+          umma_commit(&bempty[sb]);
         }
         if (!alive) break;
         umma_commit(&tfull[buf]);
@@ -347,13 +375,13 @@ __global__ void __launch_bounds__(kMxThreads, 1)
         row_src(u, gt + 64 * j, cd, ssrc[j]);
       }
       for (int ks = 0; ks < KS; ++ks, ++it) {
-        const int s = it % kMxOpStages;
-        const uint32_t ph = (it / kMxOpStages) & 1u;
-        if (!mbar_wait(&oempty[s], ph ^ 1u, abort_flag, p.err)) {
+        const int s = it % kMxAStages;
+        const uint32_t ph = (it / kMxAStages) & 1u;
+        if (!mbar_wait(&aempty[s], ph ^ 1u, abort_flag, p.err)) {
           alive = false;
           break;
         }
-        const uint32_t tile = smem_u32(op + s * kMxOp);
+        const uint32_t tile = smem_u32(atile + s * kMxA);
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const int r = (gt >> 3) + 8 * i;
@@ -382,11 +410,12 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     bool alive = true;
     for (int uu = blockIdx.x; alive && uu < num_units; uu += gridDim.x) {
       for (int ks = 0; ks < KS; ++ks, ++it) {
-        const int s = it % kMxOpStages, ws = it % kMxRawStages;
-        const uint32_t ph = (it / kMxOpStages) & 1u, wph = (it / kMxRawStages) & 1u;
-        bool ok = mbar_wait(&oempty[s], ph ^ 1u, abort_flag, p.err);
+        const int sa = it % kMxAStages, sb = it % kMxBStages, ws = it % kMxRawStages;
+        const uint32_t aph = (it / kMxAStages) & 1u, bph = (it / kMxBStages) & 1u,
+                       wph = (it / kMxRawStages) & 1u;
+        bool ok = mbar_wait(&bempty[sb], bph ^ 1u, abort_flag, p.err);
         ok = ok && mbar_wait(&wfull[ws], wph, abort_flag, p.err);
-        if (token_sf) ok = ok && mbar_wait(&afull[s], ph, abort_flag, p.err);
+        if (token_sf) ok = ok && mbar_wait(&afull[sa], aph, abort_flag, p.err);
         // the warp stops as one (its lanes meet in the warp-wide TMEM stores)
         if (__any_sync(0xffffffffu, !ok)) {
           alive = false;
@@ -396,7 +425,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
         const uint32_t rsrc = smem_u32(raw + ws * kMxRawW) + row * 64 + half * 32;
         const uint4 w0 = ld_shared_v4(rsrc), w1 = ld_shared_v4(rsrc + 16);
         const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-        const uint32_t bt = smem_u32(op + s * kMxOp + kMxA) + row * 128;
+        const uint32_t bt = smem_u32(btile + sb * kMxB) + row * 128;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const uint2 lo = e2m1x8_to_e4m3x8(words[2 * j]);
@@ -404,11 +433,11 @@ __global__ void __launch_bounds__(kMxThreads, 1)
           const int c = 4 * half + j;
           st_shared_v4(bt + ((c ^ (row & 7)) << 4), lo.x, lo.y, hi.x, hi.y);
         }
-        const uint32_t sf_col = kMxSfCol0 + 8 * s;
+        const uint32_t sf_col = kMxSfCol0 + 8 * sb;
         if (token_sf) {
           // token row 32q + lane: lane 32q + lane, column sf_col + q
           tmem_st1(lane_base + sf_col + q,
-                   ld_shared_u32(smem_u32(sfa + s * 128 + q * 32 + lane)));
+                   ld_shared_u32(smem_u32(sfa + sa * 128 + q * 32 + lane)));
         } else {
           // weight row 32c + lane: lane (mod 32) of every quarter, column sf_col + 4 + c
           const uint32_t* w = sfb + ws * kMxNT;
@@ -419,7 +448,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive(&ready[s]);
+          mbar_arrive(&ready[sb]);
           mbar_arrive(&wempty[ws]);
         }
       }
