@@ -192,16 +192,33 @@ class L2Flush:
         self.torch.sum(self.r, (0,), dtype=self.torch.int64, out=self.acc)
 
 
-def roofline_of(bytes_, flops, seconds, peaks):
+# DRAM bytes (read + write) per launch of a dominant kernel, from one ncu
+# capture of the same workload and kernel build (the profile that records it);
+# an entry is dropped whenever its kernel changes.
+MEASURED_TRAFFIC = {
+    ("qwen3", 4096, "ffn_gemm_kernel<0,128>"): (966.0e6, "profiles/ffn_gemm_qwen3_T4096.md"),
+    ("v4lo", 4096, "lowbit_gemm_kernel<0>"): (2340.0e6, "profiles/lowbit_gemm_v4lo_T4096.md"),
+}
+
+# nominal dense-rate ratio fp8 : bf16 on the tensor cores (4.5 : 2.25 PFLOP/s)
+FP8_OVER_BF16 = 2.0
+
+
+def roofline_of(bytes_, flops, seconds, peaks, fp8=False):
+    """Binding roofline of a kernel or the layer.  The tensor peak is the
+    measured bf16 figure, times the nominal fp8/bf16 ratio for the block-scaled
+    fp8 contractions of the low-bit workload."""
+    tc = peaks["bf16_tflops"] * (FP8_OVER_BF16 if fp8 else 1.0)
     t_hbm = bytes_ / (peaks["hbm_gbs"] * 1e9)
-    t_tc = flops / (peaks["bf16_tflops"] * 1e12)
+    t_tc = flops / (tc * 1e12)
     if t_hbm >= t_tc:
         ach = bytes_ / seconds / 1e9
         return {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": ach / peaks["hbm_gbs"]}
     ach = flops / seconds / 1e12
-    return {"bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-            "frac": ach / peaks["bf16_tflops"]}
+    return {"bound": "tensor", "achieved": ach, "peak": tc, "unit": "TFLOP/s",
+            "frac": ach / tc, "tensor_dtype": "fp8 (bf16 measured x 2, nominal ratio)" if fp8
+            else "bf16"}
 
 
 # --------------------------------------------------------------------------
@@ -387,15 +404,20 @@ def run_ours(args):
     stage_ms = {n: sum(v) / len(v) for n, v in per_stage.items()}
     st_model, layer_model = work_model(w, T, touched, BM)
     dom = max(names, key=lambda n: stage_ms[n])
-    roof = roofline_of(st_model[dom]["bytes"], st_model[dom]["flops"], stage_ms[dom] / 1e3, peaks)
+    roof = roofline_of(st_model[dom]["bytes"], st_model[dom]["flops"], stage_ms[dom] / 1e3, peaks,
+                       fp8=w.lowbit and dom in ("gemm1", "gemm2"))
     gk = ("lowbit_gemm_kernel<%d>", "lowbit_gemm_kernel<%d>") if w.lowbit else \
         ("ffn_gemm_kernel<%d," + str(BM) + ">", "ffn_gemm_kernel<%d," + str(BM) + ">")
     roof["kernel"] = {"router": "router_kernel", "align": "align_kernel",
                       "gemm1": gk[0] % 0, "gemm2": gk[1] % 1,
                       "finalize": "finalize_kernel"}[dom]
-    roof["traffic"] = None
+    tr = MEASURED_TRAFFIC.get((w.name, T, roof["kernel"]))
+    roof["traffic"] = tr[0] if tr else None
+    roof["traffic_unit"] = "bytes per launch"
+    roof["traffic_source"] = tr[1] if tr else None
     roof["peak_source"] = peaks["source"] + " (burst)"
-    layer_roof = roofline_of(layer_model["bytes"], layer_model["flops"], ms_per_step / 1e3, peaks)
+    layer_roof = roofline_of(layer_model["bytes"], layer_model["flops"], ms_per_step / 1e3, peaks,
+                             fp8=w.lowbit)
     del graphs, keep_alive
 
     # ---- sweep over T: per-kernel times, L2 flushed before each replay ----
@@ -443,7 +465,7 @@ def run_ours(args):
             tot = statistics.median(lt)
             del lg
             sm_, lm = work_model(w, Ts, fs["touched"], fs["block_m"])
-            lr = roofline_of(lm["bytes"], lm["flops"], tot / 1e6, peaks)
+            lr = roofline_of(lm["bytes"], lm["flops"], tot / 1e6, peaks, fp8=w.lowbit)
             sweep[str(Ts)] = {"us_per_layer": round(tot, 2),
                               "tokens_per_s": round(Ts / (tot / 1e6), 1),
                               "stage_us": {n: round(v, 2) for n, v in us.items()},

@@ -33,6 +33,22 @@ def test_roofline_picks_binding_resource():
     assert r["frac"] == pytest.approx(0.5)
     r = bench.roofline_of(1e3, 1e15, 2.0, peaks)
     assert r["bound"] == "tensor" and r["frac"] == pytest.approx(0.5)
+    # block-scaled fp8 contractions: twice the bf16 rate
+    r = bench.roofline_of(1e3, 1e15, 2.0, peaks, fp8=True)
+    assert r["bound"] == "tensor" and r["peak"] == 2000.0 and r["frac"] == pytest.approx(0.25)
+    # the binding resource moves with the faster tensor rate
+    r = bench.roofline_of(1.5e9, 2e12, 1.0, peaks, fp8=True)
+    assert r["bound"] == "hbm"
+
+
+def test_lowbit_work_model_bytes():
+    # V4-Flash low-bit: e2m1 weights with a UE8M0 byte per 32 (0.5 + 1/32 bytes
+    # per weight), e4m3 activations with a byte per 32, fp32 gate
+    w = W.WORKLOADS["v4lo"]
+    st, layer = bench.work_model(w, 1, touched=6, block_m=16)
+    w13 = 2 * w.F * w.H * (0.5 + 1 / 32)
+    assert st["gemm1"]["bytes"] == pytest.approx(6 * w13 + w.H * (1 + 1 / 32) + 6 * w.F * (1 + 1 / 32))
+    assert st["router"]["bytes"] == pytest.approx(w.E * w.H * 4 + w.H * (1 + 1 / 32) + 8 * 6)
 
 
 def test_touched_expert_model():
