@@ -103,3 +103,25 @@ def test_lowbit_layer_matches_oracle(T, ntok):
     print(f"low-bit layer T={T}: {len(tokens)} tokens, rel err {err:.2e}")
     assert len(tokens) > 0 and np.isfinite(got).all()
     assert err <= LAYER_RTOL_LOWBIT
+
+
+# Small low-bit shapes: one 64-feature GEMM1 tile and one 128-column GEMM2 tile
+# (H = 128, F = 128), several tiles with a ragged last block, BLOCK_M 16/64/128.
+@pytest.mark.parametrize("T,E,k,H,F,BM", [(5, 8, 2, 128, 128, 16), (40, 8, 2, 256, 128, 16),
+                                          (300, 16, 4, 256, 256, 64),
+                                          (700, 8, 2, 384, 128, 128)])
+def test_lowbit_small_shapes(T, E, k, H, F, BM):
+    w = W.Workload("lb", H=H, E=E, k=k, F=F, scoring="sigmoid", bias=True, lowbit=True)
+    d = W.make_inputs(w, T, seed=T, device="cuda")
+    ids, wts = W.random_routing(T, k, E, seed=T)
+    s, b, n = moe.align(ids.cuda(), E, BM)
+    out = moe.grouped_ffn(d["hidden"], d["w13"], d["w2"], k, BM, s, b, n, wts.cuda(),
+                          x_scale=d["hidden_scale"], w13_scale=d["w13_scale"],
+                          w2_scale=d["w2_scale"])
+    y = moe.finalize(out, T, k)
+    torch.cuda.synchronize()
+    tokens = np.arange(T, dtype=np.int32)
+    ref = oracle_ffn_lowbit(d, tokens, ids.numpy(), wts.numpy(), w)
+    err = rel_err(y.float().cpu().numpy(), ref)
+    print(f"low-bit T={T} E={E} k={k} H={H} F={F} BM={BM}: rel err {err:.2e}")
+    assert err <= LAYER_RTOL_LOWBIT

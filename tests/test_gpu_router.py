@@ -58,3 +58,40 @@ def test_router_zero_tokens_is_noop():
     x = torch.zeros((0, 64), dtype=torch.bfloat16, device="cuda")
     ids, wts = moe.router(x, g, None, 2)
     assert ids.shape == (0, 2)
+
+
+# Shapes around the tensor-core (tiled) router: the first tiled T, ragged
+# 128-token tiles, one or two K splits, E from 16 to 512 (two MMAs of E/2
+# above 256), bf16 and e4m3/fp32 operands.  Oracle on every token.
+SMALL = [
+    W.Workload("t1", H=128, E=64, k=4, F=0, scoring="softmax"),
+    W.Workload("t2", H=256, E=288, k=8, F=0, scoring="sigmoid", bias=True),
+    W.Workload("t3", H=192, E=16, k=2, F=0, scoring="softmax", renormalize=False, scaling=1.5),
+    W.Workload("t4", H=256, E=512, k=16, F=0, scoring="sigmoid", bias=True, n_group=8,
+               topk_group=4),
+    W.Workload("t5", H=256, E=32, k=4, F=0, scoring="sigmoid", bias=True, lowbit=True),
+]
+
+
+@pytest.mark.parametrize("wi", range(len(SMALL)))
+@pytest.mark.parametrize("T", [255, 256, 257, 300, 1000])
+def test_tiled_router_shapes(wi, T):
+    w = SMALL[wi]
+    d = W.make_inputs(w, T, seed=T + wi, device="cuda", experts=False)
+    ids, wts = moe.router(d["hidden"], d["gate"], d.get("bias"), w.k, w.scoring, w.n_group,
+                          w.topk_group, w.renormalize, w.scaling,
+                          hidden_scale=d.get("hidden_scale"))
+    torch.cuda.synchronize()
+    tokens = np.arange(T, dtype=np.int32)
+    ids_o, w_o, gap = oracle_router(oracle, w, d, T, tokens)
+    ids_g = ids.cpu().numpy()
+    w_g = wts.cpu().numpy()
+    clear = gap > GAP_MIN
+    same = (ids_g == ids_o).all(axis=1)
+    assert same[clear].all(), np.nonzero(clear & ~same)
+    assert np.abs(w_g[same] - w_o[same]).max() <= WEIGHT_ATOL
+    assert clear.mean() > 0.5
+    x_dt = "e4m3" if w.lowbit else "bf16"
+    g_dt = "f32" if w.lowbit else "bf16"
+    assert moe.router_kernel_count(T, w.H, w.E, x_dt, g_dt) == (
+        1 if T < 256 else (3 if w.lowbit else 2))
