@@ -545,7 +545,11 @@ def run_ours(args):
         import oracle
         oracle.build()
         dh = host_inputs(d)
-        n_tok = args.cpu_tokens
+        # a pilot pass sizes the sample to about 15 s of CPU work
+        pilot = min(T, 16)
+        tp = time_oracle(w, dh, T, pilot, steps=1, seed=2)[0]
+        n_tok = int(max(pilot, min(T, args.cpu_tokens if args.cpu_tokens > 0 else
+                                   pilot * 15.0 / max(tp, 1e-6))))
         times = time_oracle(w, dh, T, n_tok, steps=1, seed=1)
         cpu = {"value": round(n_tok / times[0], 3), "unit": UNIT, "cores": oracle.num_threads(),
                "kind": "oracle",
@@ -600,11 +604,12 @@ def run_reference(args):
     T = args.T
     d = W.make_inputs(w, T, seed=args.seed, device="cpu")
     dh = host_inputs(d)
-    # size the per-step sample so that warm-up + K steps take about two minutes
+    # size the per-step sample so that the W warm-up and K timed steps take
+    # about two minutes together
     t1 = time_oracle(w, dh, T, 1, steps=1, seed=100)[0]
-    budget = 120.0 / max(1, args.steps + 1)
-    n_tok = int(max(1, min(args.ref_tokens, budget // max(t1, 1e-6))))
-    time_oracle(w, dh, T, n_tok, steps=1, seed=101)
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    n_tok = int(max(1, min(T, args.ref_tokens, budget // max(t1, 1e-6))))
+    time_oracle(w, dh, T, n_tok, steps=args.warmup, seed=101)
     times = time_oracle(w, dh, T, n_tok, steps=args.steps, seed=0)
     tot = sum(times)
     value = n_tok * len(times) / tot
@@ -636,7 +641,8 @@ def main(argv=None):
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
-    ap.add_argument("--cpu-tokens", type=int, default=256)
+    ap.add_argument("--cpu-tokens", type=int, default=0,
+                    help="oracle sample size for cpu_baseline (0: about 15 s of CPU work)")
     ap.add_argument("--ref-tokens", type=int, default=32)
     args = ap.parse_args(argv)
     if args.warmup < 3:
