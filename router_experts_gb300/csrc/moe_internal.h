@@ -33,7 +33,8 @@ struct RouterPlan {
   int ne;         // expert tiles
   int nt;         // token tiles of 16
   int ks;         // K splits across CTAs
-  // tiled tensor-core path (many tokens; bf16 or e4m3 hidden, bf16 or fp32 gate)
+  // tiled tensor-core path (bf16 or e4m3 hidden, bf16 or fp32 gate)
+  int T;
   bool tiled;
   int tnt;        // token tiles of 128
   int tks;        // K splits across CTAs

@@ -34,7 +34,11 @@ namespace {
 constexpr int kRouterThreads = 256;
 constexpr int kMaxSlotsPerLane = 16;  // E <= 512
 constexpr int kTargetCtas = 304;      // two CTAs per SM of a 152-SM part
-constexpr int kTiledMinTokens = 256;  // tokens from which the tiled path is used
+// The tiled tensor-core path is used from the first token for bf16 gates and
+// from 8 tokens for fp32 gates (whose three-plane conversion launch costs more
+// than it saves on fewer tokens); measured on GB300 against the one-launch
+// kernel at T = 1 .. 255 with L2 flushed.
+constexpr int kTiledMinTokensF32Gate = 8;
 
 struct RouterArgs {
   const void* x;
@@ -284,26 +288,41 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(const RouterArgs
 #pragma unroll
     for (int c = 0; c < 4; ++c) acc[j][c] = 0.f;
 
-  for (int st = warp; st < nsteps; st += 8) {
-    const int h = (step0 + st) * 32 + 8 * q;
-    Pieces<XP> xa, xb;  // rows g and g + 8 of the token tile
-    load8<XDT>(a.x, a.x_scale, t0 + g, a.T, a.H, h, xa);
-    load8<XDT>(a.x, a.x_scale, t0 + g + 8, a.T, a.H, h, xb);
+  // U of the warp's K steps are loaded before any of them is multiplied, so
+  // their global round trips overlap (U from the registers the fragments take)
+  constexpr int kFragRegs = (2 * XP + GP * NB8) * 4;
+  constexpr int U = (NB8 > 1) ? 1 : (kFragRegs * 4 <= 64 ? 4 : (kFragRegs * 2 <= 64 ? 2 : 1));
+  for (int st0 = warp; st0 < nsteps; st0 += 8 * U) {
+    Pieces<XP> xa[U], xb[U];  // rows g and g + 8 of the token tile
+    Pieces<GP> gb[U][NB8];
 #pragma unroll
-    for (int j = 0; j < NB8; ++j) {
-      Pieces<GP> gb;
-      load8<GDT>(a.gate, nullptr, e0 + 8 * j + g, a.E, a.H, h, gb);
-      // product pieces (px, pg) with px + pg <= 2; each 32-wide step is two
-      // k16 MMAs over a permutation of the step's K indices shared by A and B
+    for (int u = 0; u < U; ++u) {
+      const int st = st0 + 8 * u;
+      if (st < nsteps) {
+        const int h = (step0 + st) * 32 + 8 * q;
+        load8<XDT>(a.x, a.x_scale, t0 + g, a.T, a.H, h, xa[u]);
+        load8<XDT>(a.x, a.x_scale, t0 + g + 8, a.T, a.H, h, xb[u]);
 #pragma unroll
-      for (int px = 0; px < XP; ++px) {
+        for (int j = 0; j < NB8; ++j) load8<GDT>(a.gate, nullptr, e0 + 8 * j + g, a.E, a.H, h, gb[u][j]);
+      }
+    }
 #pragma unroll
-        for (int pg = 0; pg < GP; ++pg) {
-          if (px + pg > 2) continue;
-          mma_bf16_16816(acc[j], xa.r[px][0], xb.r[px][0], xa.r[px][1], xb.r[px][1],
-                         gb.r[pg][0], gb.r[pg][1]);
-          mma_bf16_16816(acc[j], xa.r[px][2], xb.r[px][2], xa.r[px][3], xb.r[px][3],
-                         gb.r[pg][2], gb.r[pg][3]);
+    for (int u = 0; u < U; ++u) {
+      if (st0 + 8 * u >= nsteps) break;
+#pragma unroll
+      for (int j = 0; j < NB8; ++j) {
+        // product pieces (px, pg) with px + pg <= 2; each 32-wide step is two
+        // k16 MMAs over a permutation of the step's K indices shared by A and B
+#pragma unroll
+        for (int px = 0; px < XP; ++px) {
+#pragma unroll
+          for (int pg = 0; pg < GP; ++pg) {
+            if (px + pg > 2) continue;
+            mma_bf16_16816(acc[j], xa[u].r[px][0], xb[u].r[px][0], xa[u].r[px][1],
+                           xb[u].r[px][1], gb[u][j].r[pg][0], gb[u][j].r[pg][1]);
+            mma_bf16_16816(acc[j], xa[u].r[px][2], xb[u].r[px][2], xa[u].r[px][3],
+                           xb[u].r[px][3], gb[u][j].r[pg][2], gb[u][j].r[pg][3]);
+          }
         }
       }
     }
@@ -688,7 +707,8 @@ RouterPlan plan_router(int T, int H, int E, bool allow_tiled) {
     p.ks *= 2;
   p.scratch_bytes = align_up(static_cast<size_t>(p.ks) * T * E * sizeof(float), 256);
   // tiled path: T >= 256, E a multiple of 16 that one or two MMAs cover
-  p.tiled = allow_tiled && T >= kTiledMinTokens && H % kRgBK == 0 && E >= 16 && E % 16 == 0 &&
+  p.T = T;
+  p.tiled = allow_tiled && T >= 1 && H % kRgBK == 0 && E >= 16 && E % 16 == 0 &&
             (E <= 256 || (E <= 512 && E % 32 == 0));
   if (p.tiled) {
     p.tnt = (T + 127) / 128;
@@ -705,7 +725,8 @@ RouterPlan plan_router(int T, int H, int E, bool allow_tiled) {
 }
 
 bool router_uses_tiled(const RouterPlan& plan, int hidden_dt, int gate_dt) {
-  return plan.tiled && (hidden_dt == 0 || hidden_dt == 2) && (gate_dt == 0 || gate_dt == 1);
+  return plan.tiled && (hidden_dt == 0 || hidden_dt == 2) &&
+         (gate_dt == 0 || (gate_dt == 1 && plan.T >= kTiledMinTokensF32Gate));
 }
 
 int launch_router(const void* hidden, int hidden_dt, const uint8_t* hidden_scale,

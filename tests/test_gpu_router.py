@@ -93,5 +93,30 @@ def test_tiled_router_shapes(wi, T):
     assert clear.mean() > 0.5
     x_dt = "e4m3" if w.lowbit else "bf16"
     g_dt = "f32" if w.lowbit else "bf16"
-    assert moe.router_kernel_count(T, w.H, w.E, x_dt, g_dt) == (
-        1 if T < 256 else (3 if w.lowbit else 2))
+    assert moe.router_kernel_count(T, w.H, w.E, x_dt, g_dt) == (3 if w.lowbit else 2)
+
+
+# The one-launch kernel: fp32 hidden rows, E not a multiple of 16, and fp32
+# gates below 8 tokens.
+@pytest.mark.parametrize("name,T,f32_hidden", [("qwen3", 1, True), ("qwen3", 64, True),
+                                               ("dsv3", 200, True), ("glm", 9, True),
+                                               ("v4lo", 1, False), ("v4lo", 7, False)])
+def test_one_launch_router(name, T, f32_hidden):
+    w = W.WORKLOADS[name]
+    d = W.make_inputs(w, T, seed=T, device="cuda", experts=False)
+    x = d["hidden"].float() if f32_hidden else d["hidden"]
+    g_dt = "f32" if w.lowbit else "bf16"
+    x_dt = "f32" if f32_hidden else ("e4m3" if w.lowbit else "bf16")
+    assert moe.router_kernel_count(T, w.H, w.E, x_dt, g_dt) == 1
+    ids, wts = moe.router(x, d["gate"], d.get("bias"), w.k, w.scoring, w.n_group,
+                          w.topk_group, w.renormalize, w.scaling,
+                          hidden_scale=d.get("hidden_scale"))
+    torch.cuda.synchronize()
+    tokens = np.arange(T, dtype=np.int32)
+    ids_o, w_o, gap = oracle_router(oracle, w, d, T, tokens)
+    ids_g, w_g = ids.cpu().numpy(), wts.cpu().numpy()
+    clear = gap > GAP_MIN
+    same = (ids_g == ids_o).all(axis=1)
+    assert same[clear].all(), np.nonzero(clear & ~same)
+    assert np.abs(w_g[same] - w_o[same]).max() <= WEIGHT_ATOL
+    assert clear.any()
