@@ -79,21 +79,20 @@ struct Cfg {
 };
 
 // Split count for the swap tiles: minimise (waves x k-blocks per unit) with a
-// per-unit overhead of one k-block, within the partial-sum capacity.
+// per-unit overhead of one k-block, within the partial-sum capacity.  Lane l of
+// the calling warp evaluates s = l + 1 (every lane must call); ties go to the
+// fewest splits.  32-bit arithmetic: every product stays below 2^31.
 MOE_DEV int choose_splits(int ug, int KB, int ctas, int max_slots) {
-  if (ug <= 0) return 1;
-  int best_s = 1;
-  long long best = 0x7fffffffffffffffll;
-  for (int s = 1; s <= 32 && s <= KB; ++s) {
-    if (s > 1 && static_cast<long long>(ug) * s > max_slots) break;
-    const long long waves = (static_cast<long long>(ug) * s + ctas - 1) / ctas;
-    const long long cost = waves * ((KB + s - 1) / s + 1);
-    if (cost < best) {
-      best = cost;
-      best_s = s;
-    }
+  const int lane = threadIdx.x & 31;
+  const int s = lane + 1;
+  uint32_t key = 0xFFFFFFFFu;
+  if (ug > 0 && s <= KB && (s == 1 || ug * s <= max_slots)) {
+    const int waves = (ug * s + ctas - 1) / ctas;
+    const int cost = waves * ((KB + s - 1) / s + 1);
+    key = (static_cast<uint32_t>(min(cost, (1 << 26) - 1)) << 5) | static_cast<uint32_t>(lane);
   }
-  return best_s;
+  key = __reduce_min_sync(0xffffffffu, key);
+  return (key == 0xFFFFFFFFu) ? 1 : static_cast<int>(key & 31u) + 1;
 }
 
 struct Sched {
@@ -129,8 +128,8 @@ MOE_DEV Unit decode_unit(const FfnParams& p, const Sched& sc, int u) {
   x.ug = u / sc.S;
   x.b = x.ug / sc.ntiles;
   x.n = x.ug % sc.ntiles;
-  x.kb0 = static_cast<int>(static_cast<long long>(x.s) * sc.KB / sc.S);
-  x.kb1 = static_cast<int>(static_cast<long long>(x.s + 1) * sc.KB / sc.S);
+  x.kb0 = x.s * sc.KB / sc.S;  // KB <= 2^16 and s <= 32: no overflow
+  x.kb1 = (x.s + 1) * sc.KB / sc.S;
   int e = __ldg(p.block_expert + x.b);
   if (e < 0 || e >= p.E) {
     if (threadIdx.x == 0) raise_error(p.err, kErrBadTable);
