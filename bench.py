@@ -298,6 +298,17 @@ def run_ours(args):
 
     # ---- stage graphs (each holds exactly one kernel of the library) ----
     ws = moe.Workspace(dev)
+    # One workspace, sized once for every call below: a CUDA graph keeps the
+    # buffer it was captured with, so the buffer must never be replaced.
+    lib = moe.load()
+    adt = moe.DT_E4M3 if w.lowbit else moe.DT_BF16
+    ws_need = 0
+    for Tn in set([T] + list(w.Ts)):
+        bmn = moe.pick_block_m(Tn, k, E)
+        ws_need = max(ws_need, moe.layer_workspace_bytes(Tn, H, F, E, k, 0, adt),
+                      lib.moe_router_workspace_bytes(Tn, H, E), lib.moe_align_workspace_bytes(),
+                      lib.moe_ffn_workspace_bytes(Tn, H, F, E, k, bmn, adt))
+    ws.get(ws_need)
     names = ["router", "align", "gemm1", "gemm2", "finalize"]
 
     def stage_graphs(x, xs=None):

@@ -194,10 +194,12 @@ int moe_align(const int32_t* topk_ids, int T, int k, int E, int block_m, int32_t
  *   codes, inter_scale [cap_rows,F/32] (written by gemm1: [P4] §3.5 scale =
  *   smallest power of two with amax/scale <= 448, codes rounded to nearest
  *   even and saturated at 448); w2 [E,H,F/2] e2m1, w2_scale [E,H,F/32].
- *   Products are formed exactly (f16 operands, fp32 accumulation) when every
- *   scale exponent s-127 lies in [-14, 13] for weights and [-14, 7] for
- *   activations; exponents outside [-14, 15] are clamped, so such inputs
- *   give results that differ from the exact dequantised product.
+ *   w13 and w2 must be 32-byte aligned, the other low-bit arrays 16-byte
+ *   (codes) or 4-byte (scales) aligned (MOE_ERR_ARG otherwise).
+ *   The tensor core applies every scale byte as an exact power of two and
+ *   accumulates in fp32, so the result is the dequantised product up to fp32
+ *   accumulation rounding while the scaled values stay in the fp32 normal
+ *   range.
  * ------------------------------------------------------------------------- */
 size_t moe_ffn_workspace_bytes(int T, int H, int F, int E, int k, int block_m, int act_dt);
 int moe_expert_gemm1(const void* x, int act_dt, const uint8_t* x_scale, const void* w13,

@@ -125,7 +125,8 @@ __global__ void __launch_bounds__(kAlignThreads) align_kernel(const AlignArgs a)
 
   // 2. totals and this CTA's base per expert
   if (a.G > 1) {
-    grid_barrier(a.bar, a.G, a.err);
+    // on a timed-out barrier the table is incomplete: write nothing
+    if (!grid_barrier(a.bar, a.G, a.err)) return;
     for (int e = tid; e < E; e += kAlignThreads) {
       int t = 0, b = 0;
       for (int c0 = 0; c0 < a.G; c0 += 8) {
@@ -199,7 +200,7 @@ __global__ void __launch_bounds__(kAlignThreads) align_kernel(const AlignArgs a)
       __syncwarp();
       if (e >= 0) {
         const int pos = pos0 + __popc(m & lt_mask);
-        a.sorted[pos] = p;
+        if (pos >= 0 && pos < a.cap) a.sorted[pos] = p;
         if (lane == __ffs(m) - 1) cnt[warp * E + e] = pos0 + __popc(m);
       }
       __syncwarp();
@@ -209,15 +210,20 @@ __global__ void __launch_bounds__(kAlignThreads) align_kernel(const AlignArgs a)
   // 4. fill, split over every warp of the grid: each expert's pad rows and
   // blocks, then the tail of sorted_ids and of the block table
   const int gw = c * kAlignWarps + warp, nw = a.G * kAlignWarps;
+  // (every write is bounded by the buffer sizes, so a table corrupted
+  // outside this kernel cannot send a write out of range)
   for (int e = gw; e < E; e += nw) {
     const int s = start[e], t = tot[e], pd = (t + BM - 1) / BM * BM;
-    for (int p = s + t + lane; p < s + pd; p += 32) a.sorted[p] = a.n;
-    for (int b = s / BM + lane; b < (s + pd) / BM; b += 32) a.blk[b] = e;
+    for (int p = s + t + lane; p < s + pd; p += 32)
+      if (p >= 0 && p < a.cap) a.sorted[p] = a.n;
+    for (int b = s / BM + lane; b < (s + pd) / BM; b += 32)
+      if (b >= 0 && b < a.nbc) a.blk[b] = e;
   }
   const long long gt = static_cast<long long>(c) * kAlignThreads + tid;
   const long long nt = static_cast<long long>(a.G) * kAlignThreads;
-  for (long long p = total + gt; p < a.cap; p += nt) a.sorted[p] = a.n;
-  for (long long b = total / BM + gt; b < a.nbc; b += nt) a.blk[b] = -1;
+  const long long tail = total < 0 ? 0 : total;
+  for (long long p = tail + gt; p < a.cap; p += nt) a.sorted[p] = a.n;
+  for (long long b = tail / BM + gt; b < a.nbc; b += nt) a.blk[b] = -1;
   if (c == 0 && tid == 0) *a.npp = total;
 }
 

@@ -289,7 +289,7 @@ static int expert_gemm_lowbit(int kind, const void* act, const uint8_t* act_scal
     return MOE_ERR_ARG;
   if (kind == 0 && (!inter_q || !inter_scale)) return MOE_ERR_ARG;
   if (kind == 1 && (!topk_weights || !stage)) return MOE_ERR_ARG;
-  if (!aligned(act, 16) || !aligned(w, 16) || !aligned(act_scale, 4) || !aligned(w_scale, 4) ||
+  if (!aligned(act, 16) || !aligned(w, 32) || !aligned(act_scale, 4) || !aligned(w_scale, 4) ||
       (inter_q && !aligned(inter_q, 32)) || (inter_scale && !aligned(inter_scale, 4)) ||
       (stage && !aligned(stage, 32)))
     return MOE_ERR_ARG;

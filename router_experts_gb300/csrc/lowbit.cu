@@ -10,31 +10,34 @@
 // sorted_ids, gather folded into the load, weight in the down GEMM's
 // epilogue).
 //
-// The products run on the block-scaled tensor-core MMA
-// (tcgen05.mma kind::mxf8f6f4 with one UE8M0 scale per 32 values of each
-// operand row, fp32 accumulation in TMEM), so the scales are applied by the
-// tensor core and the operands stay one byte wide in shared memory:
-//   A = 128 token rows of e4m3 codes, gathered as they are (no conversion);
-//   B = 128 weight rows, e2m1 codes widened to e4m3 (exact: every e2m1 value
-//       is an e4m3 value) by converter warps;
-//   scale factors are written to TMEM with tcgen05.st: for row m of A, lane m
-//   and column base + m/32; for row n of B, lane n mod 32 (in every lane
-//   quarter) and column base + n/32; byte j of the word scales the j-th
-//   32-value block of a 128-value K step.
+// The products run on the block-scaled tensor-core MMA (tcgen05.mma
+// kind::mxf8f6f4, A = e4m3, B = e2m1, one UE8M0 scale per 32 values of each
+// operand row, fp32 accumulation in TMEM).  Nothing is converted on the SMs:
+//   B = 128 weight rows, loaded by TMA straight from the packed e2m1 codes
+//       with the 16 x 4-bit / 16-byte tensor-map type: each 16 codes land as
+//       their 8 packed bytes plus an 8-byte gap, the MMA's 4-bit operand
+//       layout (the copy counts the packed bytes in its transactions);
+//   A = 128 token rows of e4m3 codes: GEMM1 gathers them by sorted_ids with
+//       cp.async, GEMM2 reads its contiguous intermediate rows by TMA;
+//   scale words (4 K-blocks of one row) are copied into a [32][4]-word image
+//       per operand (word c of image row l = operand row 32c + l) and moved
+//       to TMEM by the MMA thread with tcgen05.cp 32x128b.warpx4, which puts
+//       image row l in lane l of every lane quarter: row m of A reads lane m,
+//       column base + m/32; row n of B reads lane n mod 32, column base + 4 +
+//       n/32; byte j of the word scales K-block j of the step.
 // Tile: M = 128 token rows of one block (BLOCK_M rows valid), N = 128 weight
 // rows (GEMM1: 64 gate rows + the matching 64 up rows), K steps of 128 (four
-// K=32 MMAs).  Two 128-column accumulators, double-buffered.
-// 16 warps:
-//   warp 0      TMA of the packed weight codes (ring of 6 raw stages, L2
-//               warmed one ring ahead) and,
-//               one row per lane, cp.async of their scale words
-//   warp 1      TMEM allocation and the single thread issuing the MMAs
-//   warps 2-3   cp.async gather of the token codes and scale words straight
-//               into the token-tile ring (6 deep: it covers the gather latency)
-//   warps 4-11  widen the weight codes into the weight-tile ring (4 deep); warps 4-7
-//               write the token scale factors to TMEM, warps 8-11 the weight
-//               scale factors
-//   warps 12-15 epilogue (TMEM lane quarter = warp % 4)
+// K = 32 MMAs).  Two 128-column accumulators, double-buffered; the scale
+// words of a step sit in an 8-column TMEM slot tied to its weight stage.
+// 10 warps:
+//   warp 0      TMA of the weight tiles (L2 warmed kMxL2Ahead steps ahead
+//               through a plain byte map of the same codes)
+//               and, one row per lane, cp.async of their scale words
+//   warp 1      TMEM allocation and the single thread issuing tcgen05.cp and
+//               the MMAs
+//   warps 2-5   token tiles: GEMM1 cp.async gather of the codes and scale
+//               words; GEMM2 TMA of the codes, cp.async of the scale words
+//   warps 6-9   epilogue (TMEM lane quarter = warp % 4)
 #include <cuda_fp8.h>
 
 #include "moe_common.cuh"
@@ -44,40 +47,35 @@ namespace moe {
 
 namespace {
 
-constexpr int kMxThreads = 512;
+constexpr int kMxThreads = 320;
 constexpr int kMxBK = 128;                  // K values per stage (4 MMAs of K = 32)
 constexpr int kMxNT = 128;                  // weight rows per tile (MMA N)
-// Token tiles wait on gather latency, so their ring is deep; the widened
-// weight tiles are written just ahead of their MMAs, so theirs is short.
-constexpr int kMxAStages = 6;               // token-code tiles
-constexpr int kMxBStages = 4;               // widened weight tiles (and scale-factor slots)
-constexpr int kMxRawStages = 6;             // packed weight-code stages (streamed from HBM)
-constexpr int kMxA = 128 * kMxBK;           // 16 KB of token codes
-constexpr int kMxB = kMxNT * kMxBK;         // 16 KB of widened weight codes
-constexpr int kMxRawW = kMxNT * (kMxBK / 2);  // 8 KB of packed weight codes
-constexpr int kMxABytes = kMxAStages * kMxA;
-constexpr int kMxBBytes = kMxBStages * kMxB;
-constexpr int kMxRawBytes = kMxRawStages * kMxRawW;
-constexpr int kMxSfaBytes = kMxAStages * 128 * 4;      // token scale words per token tile
-constexpr int kMxSfbBytes = kMxRawStages * kMxNT * 4;  // weight scale words per raw stage
+constexpr int kMxAStages = 7;               // token tiles
+constexpr int kMxBStages = 6;               // weight tiles (and TMEM scale slots)
+constexpr int kMxL2Ahead = 12;              // weight steps warmed in L2 ahead of their load
+constexpr int kMxTile = 128 * kMxBK;        // 16 KB per tile (one byte per code in smem)
+constexpr int kMxSfImg = 128 * 4;           // 512 B: one operand's scale words of a step
 constexpr int kMxBarBytes = 512;
 constexpr int kMxSmem =
-    kMxABytes + kMxBBytes + kMxRawBytes + kMxSfaBytes + kMxSfbBytes + kMxBarBytes + 1024;
+    (kMxAStages + kMxBStages) * (kMxTile + kMxSfImg) + kMxBarBytes + 1024;
 static_assert(kMxSmem <= 232448, "shared memory budget");
 constexpr uint32_t kMxAccCols = 128;        // per accumulator buffer
-constexpr uint32_t kMxSfCol0 = 256;         // scale-factor columns: 8 per weight-tile slot
+constexpr uint32_t kMxSfCol0 = 256;         // scale slots: 8 columns per weight stage
 constexpr uint32_t kMxTmemCols = 512;
+static_assert(kMxSfCol0 + 8 * kMxBStages <= kMxTmemCols, "TMEM columns");
 
-// Instruction descriptor of the block-scaled MMA: e4m3 A and B (K-major),
-// UE8M0 scales, fp32 D; sf_id picks the scale byte of the 32-bit TMEM word.
-__host__ __device__ constexpr uint32_t idesc_mxf8(int M, int N, int sf_id) {
-  return (static_cast<uint32_t>(sf_id) << 4) | (static_cast<uint32_t>(N >> 3) << 17) |
-         (1u << 23) | (static_cast<uint32_t>(M >> 4) << 24) | (static_cast<uint32_t>(sf_id) << 29);
+// Instruction descriptor of the block-scaled MMA: e4m3 A, e2m1 B (both
+// K-major), UE8M0 scales, fp32 D; sf_id picks the scale byte of the 32-bit
+// TMEM word for both operands.
+__host__ __device__ constexpr uint32_t idesc_mxf8f4(int M, int N, int sf_id) {
+  return (static_cast<uint32_t>(sf_id) << 4) | (5u << 10) |
+         (static_cast<uint32_t>(N >> 3) << 17) | (1u << 23) |
+         (static_cast<uint32_t>(M >> 4) << 24) | (static_cast<uint32_t>(sf_id) << 29);
 }
 
 // D[tmem] (+)= (A * sa)[smem] * (B * sb)[smem]^T with per-32 UE8M0 scales in TMEM.
-MOE_DEV void umma_mxf8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                       uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+MOE_DEV void umma_mxf8f4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                         uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
   asm volatile(
       "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
       " tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, "
@@ -86,58 +84,23 @@ MOE_DEV void umma_mxf8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32
       : "memory");
 }
 
-// Warp-wide TMEM stores (lane i of the warp -> TMEM lane (address lane field + i)).
-MOE_DEV void tmem_st1(uint32_t taddr, uint32_t v) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
-}
-MOE_DEV void tmem_st4(uint32_t taddr, uint32_t v0, uint32_t v1, uint32_t v2, uint32_t v3) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr),
-               "r"(v0), "r"(v1), "r"(v2), "r"(v3)
-               : "memory");
-}
-MOE_DEV void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
-
-// 4 bytes = 8 e2m1 codes (low nibble first) -> 8 e4m3 codes (two words, in
-// order): hardware e2m1x2 -> f16x2 and f16x2 -> e4m3x2 conversions, both
-// exact on these values.
-MOE_DEV uint2 e2m1x8_to_e4m3x8(uint32_t w) {
-  uint32_t h[4];
-  asm("{\n"
-      " .reg .b8 q0, q1, q2, q3;\n"
-      " mov.b32 {q0, q1, q2, q3}, %4;\n"
-      " cvt.rn.f16x2.e2m1x2 %0, q0;\n"
-      " cvt.rn.f16x2.e2m1x2 %1, q1;\n"
-      " cvt.rn.f16x2.e2m1x2 %2, q2;\n"
-      " cvt.rn.f16x2.e2m1x2 %3, q3;\n"
-      "}"
-      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
-      : "r"(w));
-  uint32_t o[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    uint16_t b;
-    asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(b) : "r"(h[i]));
-    o[i] = b;
-  }
-  return make_uint2(o[0] | (o[1] << 16), o[2] | (o[3] << 16));
+// Shared-memory descriptor of a [32 rows x 16 bytes] image, no swizzle: one
+// 16-byte core-matrix column, row groups of 8 every 128 bytes.
+MOE_DEV uint64_t sf_image_desc(uint32_t smem_byte_addr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((smem_byte_addr & 0x3FFFFu) >> 4);  // start address
+  d |= static_cast<uint64_t>(1) << 16;                           // leading byte offset (unused)
+  d |= static_cast<uint64_t>(128 >> 4) << 32;                    // stride byte offset
+  d |= static_cast<uint64_t>(1) << 46;                           // descriptor version
+  return d;
 }
 
-MOE_DEV void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
-               "r"(d)
+// Copy a [32 x 128-bit] shared-memory image into 4 TMEM columns of every lane
+// quarter (image row l -> lanes l, 32 + l, 64 + l, 96 + l).  Ordered before
+// the MMAs the same thread issues after it.
+MOE_DEV void tmem_cp_32x128_x4(uint32_t taddr, uint64_t desc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc)
                : "memory");
-}
-MOE_DEV uint4 ld_shared_v4(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(addr));
-  return v;
-}
-MOE_DEV uint32_t ld_shared_u32(uint32_t addr) {
-  uint32_t v;
-  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
-  return v;
 }
 
 // e4m3 codes of 32 activations with their UE8M0 exponent byte: scale = the
@@ -186,21 +149,20 @@ MOE_DEV int mx_wrow(const LowbitParams& p, const MxUnit& u, int r) {
 
 template <int KIND>
 __global__ void __launch_bounds__(kMxThreads, 1)
-    lowbit_gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const LowbitParams p) {
+    lowbit_gemm_kernel(const __grid_constant__ CUtensorMap tm_w,
+                       const __grid_constant__ CUtensorMap tm_wpf,
+                       const __grid_constant__ CUtensorMap tm_a, const LowbitParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  uint8_t* atile = smem;                  // [kMxAStages][128 token rows x 128 codes]
-  uint8_t* btile = atile + kMxABytes;     // [kMxBStages][128 weight rows x 128 codes]
-  uint8_t* raw = btile + kMxBBytes;       // [kMxRawStages][128 rows x 64 bytes]
-  uint32_t* sfa = reinterpret_cast<uint32_t*>(raw + kMxRawBytes);  // [kMxAStages][128]
-  uint32_t* sfb = sfa + kMxAStages * 128;                          // [kMxRawStages][128]
-  uint64_t* wfull = reinterpret_cast<uint64_t*>(sfb + kMxRawStages * kMxNT);
-  uint64_t* wempty = wfull + kMxRawStages;
-  uint64_t* afull = wempty + kMxRawStages;
+  uint8_t* atile = smem;                              // [kMxAStages][128 rows x 128 codes]
+  uint8_t* btile = atile + kMxAStages * kMxTile;      // [kMxBStages][128 rows x 128 slots]
+  uint32_t* sfa = reinterpret_cast<uint32_t*>(btile + kMxBStages * kMxTile);  // [kMxAStages][128]
+  uint32_t* sfb = sfa + kMxAStages * 128;                                     // [kMxBStages][128]
+  uint64_t* afull = reinterpret_cast<uint64_t*>(sfb + kMxBStages * 128);
   uint64_t* aempty = afull + kMxAStages;
-  uint64_t* ready = aempty + kMxAStages;
-  uint64_t* bempty = ready + kMxBStages;
+  uint64_t* bfull = aempty + kMxAStages;
+  uint64_t* bempty = bfull + kMxBStages;
   uint64_t* tfull = bempty + kMxBStages;
   uint64_t* tempty = tfull + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
@@ -214,18 +176,16 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   const int nblk = npp / p.BM;
   const int ntiles = (KIND == 0) ? p.F / (kMxNT / 2) : p.H / kMxNT;
   const int num_units = nblk * ntiles;
+  const int bmr = min(p.BM, 128);  // token rows of a tile that hold data
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kMxRawStages; ++i) {
-      mbar_init(&wfull[i], 1 + 32);  // TMA bytes + the scale-word copies of warp 0
-      mbar_init(&wempty[i], 8);      // converter warps
-    }
     for (int i = 0; i < kMxAStages; ++i) {
-      mbar_init(&afull[i], 64);      // gather threads
-      mbar_init(&aempty[i], 1);      // MMA commit
+      // gather threads (cp.async arrivals); GEMM2 adds the TMA's expect-tx arrival
+      mbar_init(&afull[i], 128 + (KIND == 1 ? 1 : 0));
+      mbar_init(&aempty[i], 1);  // MMA commit
     }
     for (int i = 0; i < kMxBStages; ++i) {
-      mbar_init(&ready[i], 8);       // converter warps
+      mbar_init(&bfull[i], 1 + 32);  // TMA bytes + the scale-word copies of warp 0
       mbar_init(&bempty[i], 1);      // MMA commit
     }
     for (int i = 0; i < 2; ++i) {
@@ -255,51 +215,57 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   };
 
   if (warp == 0) {
-    // ---------------- packed weight codes (TMA) + their scale words ----------------
-    if (lane == 0) tma_prefetch_desc(&tm_w);
+    // ---------------- weight tiles (TMA) + their scale words ----------------
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_w);
+      tma_prefetch_desc(&tm_wpf);
+    }
     uint32_t it = 0;
     bool alive = true;
     for (int uu = blockIdx.x; alive && uu < num_units; uu += gridDim.x) {
       const MxUnit u = decode(uu);
+      // lane l copies the scale words of rows l, 32 + l, 64 + l, 96 + l: image
+      // row l, words 0..3
       const uint8_t* srow[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
-        srow[i] = p.w_scale + static_cast<size_t>(mx_wrow<KIND>(p, u, lane + 32 * i)) * (K / 32);
+      for (int c = 0; c < 4; ++c)
+        srow[c] = p.w_scale + static_cast<size_t>(mx_wrow<KIND>(p, u, lane + 32 * c)) * (K / 32);
       const int r0 = mx_wrow<KIND>(p, u, 0), r64 = mx_wrow<KIND>(p, u, 64);
-      // the next unit of this CTA, for warming L2 one raw ring ahead
+      // the next unit of this CTA, for warming L2 across the unit boundary
       const bool has_next = uu + static_cast<int>(gridDim.x) < num_units;
       const MxUnit nu = has_next ? decode(uu + gridDim.x) : u;
       const int n0 = mx_wrow<KIND>(p, nu, 0), n64 = mx_wrow<KIND>(p, nu, 64);
       for (int ks = 0; ks < KS; ++ks, ++it) {
         if (lane == 0) {
-          int pk = ks + kMxRawStages, p0 = r0, p64 = r64;
+          int pk = ks + kMxL2Ahead, p0 = r0, p64 = r64;
           if (pk >= KS && has_next) {
             pk -= KS;
             p0 = n0;
             p64 = n64;
           }
-          if (pk < KS) {
-            tma_prefetch_l2_2d(&tm_w, pk * (kMxBK / 2), p0);
-            tma_prefetch_l2_2d(&tm_w, pk * (kMxBK / 2), p64);
+          if (pk < KS) {  // byte map of the packed codes: x in bytes
+            tma_prefetch_l2_2d(&tm_wpf, pk * (kMxBK / 2), p0);
+            tma_prefetch_l2_2d(&tm_wpf, pk * (kMxBK / 2), p64);
           }
         }
-        const int ws = it % kMxRawStages;
-        const uint32_t ph = (it / kMxRawStages) & 1u;
-        const bool ok = mbar_wait(&wempty[ws], ph ^ 1u, abort_flag, p.err);
+        const int ws = it % kMxBStages;
+        const uint32_t ph = (it / kMxBStages) & 1u;
+        const bool ok = mbar_wait(&bempty[ws], ph ^ 1u, abort_flag, p.err);
         if (__any_sync(0xffffffffu, !ok)) {
           alive = false;
           break;
         }
         if (lane == 0) {
-          uint8_t* dst = raw + ws * kMxRawW;
-          mbar_arrive_expect_tx(&wfull[ws], kMxRawW);
-          tma_load_2d(dst, &tm_w, &wfull[ws], ks * (kMxBK / 2), r0);
-          tma_load_2d(dst + 64 * 64, &tm_w, &wfull[ws], ks * (kMxBK / 2), r64);
+          uint8_t* dst = btile + ws * kMxTile;
+          // two 64-row boxes of 128 codes: 2 x 64 x 64 packed bytes
+          mbar_arrive_expect_tx(&bfull[ws], kMxNT * kMxBK / 2);
+          tma_load_2d(dst, &tm_w, &bfull[ws], ks * kMxBK, r0);
+          tma_load_2d(dst + 64 * 128, &tm_w, &bfull[ws], ks * kMxBK, r64);
         }
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-          cp_async_4(smem_u32(sfb + ws * kMxNT + lane + 32 * i), srow[i] + ks * 4, 4u);
-        cp_async_mbar_arrive_noinc(&wfull[ws]);
+        for (int c = 0; c < 4; ++c)
+          cp_async_4(smem_u32(sfb + ws * 128 + 4 * lane + c), srow[c] + ks * 4, 4u);
+        cp_async_mbar_arrive_noinc(&bfull[ws]);
       }
     }
     cp_async_wait_all();
@@ -316,21 +282,25 @@ __global__ void __launch_bounds__(kMxThreads, 1)
         const uint32_t d = tmem_base + buf * kMxAccCols;
         for (int ks = 0; ks < KS; ++ks, ++it) {
           const int sa = it % kMxAStages, sb = it % kMxBStages;
-          const uint32_t bph = (it / kMxBStages) & 1u;
-          // the converters signal after the token tile of this step has landed
-          if (!mbar_wait(&ready[sb], bph, abort_flag, p.err)) {
+          if (!mbar_wait(&afull[sa], (it / kMxAStages) & 1u, abort_flag, p.err) ||
+              !mbar_wait(&bfull[sb], (it / kMxBStages) & 1u, abort_flag, p.err)) {
             alive = false;
             break;
           }
-          fence_proxy_async_smem();  // cp.async token rows -> tensor core
+          fence_proxy_async_smem();  // cp.async rows and scale words -> tensor core
           tc_fence_after();
-          const uint32_t a_addr = smem_u32(atile + sa * kMxA);
-          const uint32_t b_addr = smem_u32(btile + sb * kMxB);
-          const uint32_t sfa_t = tmem_base + kMxSfCol0 + 8 * sb;
+          // The scale slot of weight stage sb was last read by the MMAs of step
+          // it - kMxBStages, complete before that stage was refilled.
+          const uint32_t sf_t = tmem_base + kMxSfCol0 + 8 * sb;
+          tmem_cp_32x128_x4(sf_t, sf_image_desc(smem_u32(sfa + sa * 128)));
+          tmem_cp_32x128_x4(sf_t + 4, sf_image_desc(smem_u32(sfb + sb * 128)));
+          const uint32_t a_addr = smem_u32(atile + sa * kMxTile);
+          const uint32_t b_addr = smem_u32(btile + sb * kMxTile);
 #pragma unroll
           for (int kk = 0; kk < kMxBK / 32; ++kk)
-            umma_mxf8(d, sw128_desc(a_addr + kk * 32), sw128_desc(b_addr + kk * 32),
-                      idesc_mxf8(128, kMxNT, kk), sfa_t, sfa_t + 4, (ks > 0 || kk > 0) ? 1u : 0u);
+            umma_mxf8f4(d, sw128_desc(a_addr + kk * 32), sw128_desc(b_addr + kk * 32),
+                        idesc_mxf8f4(128, kMxNT, kk), sf_t, sf_t + 4,
+                        (ks > 0 || kk > 0) ? 1u : 0u);
           umma_commit(&aempty[sa]);
           umma_commit(&bempty[sb]);
         }
@@ -338,10 +308,12 @@ __global__ void __launch_bounds__(kMxThreads, 1)
         umma_commit(&tfull[buf]);
       }
     }
-  } else if (warp < 4) {
-    // ---------------- token codes + scale words (cp.async gather) ----------------
-    const int gt = threadIdx.x - 64;  // 0..63
+  } else if (warp < 6) {
+    // ---------------- token tiles + their scale words ----------------
+    const int gt = threadIdx.x - 64;  // 0..127
     const int chunk = gt & 7;
+    // image slot of row gt's scale word: image row gt % 32, word gt / 32
+    const int sf_word = 4 * (gt & 31) + (gt >> 5);
     uint32_t it = 0;
     bool alive = true;
     auto row_src = [&](const MxUnit& u, int r, const uint8_t*& codes, const uint8_t*& scales) {
@@ -360,19 +332,21 @@ __global__ void __launch_bounds__(kMxThreads, 1)
         scales = p.act_scale + prow * (K / 32);
       }
     };
+    if (KIND == 1 && gt == 0) tma_prefetch_desc(&tm_a);
     for (int uu = blockIdx.x; alive && uu < num_units; uu += gridDim.x) {
       const MxUnit u = decode(uu);
-      const uint8_t* src[16];
-      const uint8_t* ssrc[2];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const uint8_t* sc;
-        row_src(u, (gt >> 3) + 8 * i, src[i], sc);
-      }
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
+      const uint8_t* src[8];
+      const uint8_t* ssrc;
+      {
         const uint8_t* cd;
-        row_src(u, gt + 64 * j, cd, ssrc[j]);
+        row_src(u, gt, cd, ssrc);
+      }
+      if constexpr (KIND == 0) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint8_t* sc;
+          row_src(u, (gt >> 3) + 16 * i, src[i], sc);
+        }
       }
       for (int ks = 0; ks < KS; ++ks, ++it) {
         const int s = it % kMxAStages;
@@ -381,79 +355,31 @@ __global__ void __launch_bounds__(kMxThreads, 1)
           alive = false;
           break;
         }
-        const uint32_t tile = smem_u32(atile + s * kMxA);
+        if constexpr (KIND == 0) {
+          const uint32_t tile = smem_u32(atile + s * kMxTile);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int r = (gt >> 3) + 8 * i;
-          const uint32_t dst = tile + r * 128 + ((chunk ^ (r & 7)) << 4);
-          cp_async_16(dst, src[i] ? static_cast<const void*>(src[i] + ks * kMxBK + chunk * 16) : p.act,
-                      src[i] ? 16u : 0u);
+          for (int i = 0; i < 8; ++i) {
+            const int r = (gt >> 3) + 16 * i;
+            const uint32_t dst = tile + r * 128 + ((chunk ^ (r & 7)) << 4);
+            cp_async_16(dst,
+                        src[i] ? static_cast<const void*>(src[i] + ks * kMxBK + chunk * 16) : p.act,
+                        src[i] ? 16u : 0u);
+          }
+        } else {
+          // the block's rows are contiguous: one box of bmr rows
+          if (gt == 0) {
+            mbar_arrive_expect_tx(&afull[s], static_cast<uint32_t>(bmr) * kMxBK);
+            tma_load_2d(atile + s * kMxTile, &tm_a, &afull[s], ks * kMxBK, u.b * p.BM);
+          }
         }
-#pragma unroll
-        for (int j = 0; j < 2; ++j)
-          cp_async_4(smem_u32(sfa + s * 128 + gt + 64 * j),
-                     ssrc[j] ? static_cast<const void*>(ssrc[j] + ks * 4) : p.act_scale,
-                     ssrc[j] ? 4u : 0u);
+        cp_async_4(smem_u32(sfa + s * 128 + sf_word),
+                   ssrc ? static_cast<const void*>(ssrc + ks * 4) : p.act_scale, ssrc ? 4u : 0u);
         // the stage barrier counts this thread's arrival when its copies land
         cp_async_mbar_arrive_noinc(&afull[s]);
       }
     }
     cp_async_wait_all();
-  } else if (warp < 12) {
-    // ---------------- weight codes -> e4m3 operand, scale factors -> TMEM ----------------
-    const int ct = threadIdx.x - 128;  // 0..255: half (ct & 1) of weight row ct >> 1
-    const int row = ct >> 1, half = ct & 1;
-    const int q = warp & 3;            // this warp's TMEM lane quarter
-    const bool token_sf = warp < 8;    // warps 4-7: token scales, warps 8-11: weight scales
-    const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-    uint32_t it = 0;
-    bool alive = true;
-    for (int uu = blockIdx.x; alive && uu < num_units; uu += gridDim.x) {
-      for (int ks = 0; ks < KS; ++ks, ++it) {
-        const int sa = it % kMxAStages, sb = it % kMxBStages, ws = it % kMxRawStages;
-        const uint32_t aph = (it / kMxAStages) & 1u, bph = (it / kMxBStages) & 1u,
-                       wph = (it / kMxRawStages) & 1u;
-        bool ok = mbar_wait(&bempty[sb], bph ^ 1u, abort_flag, p.err);
-        ok = ok && mbar_wait(&wfull[ws], wph, abort_flag, p.err);
-        if (token_sf) ok = ok && mbar_wait(&afull[sa], aph, abort_flag, p.err);
-        // the warp stops as one (its lanes meet in the warp-wide TMEM stores)
-        if (__any_sync(0xffffffffu, !ok)) {
-          alive = false;
-          break;
-        }
-        // 32 packed bytes (64 codes) of the row -> 64 e4m3 bytes, 128-byte swizzle
-        const uint32_t rsrc = smem_u32(raw + ws * kMxRawW) + row * 64 + half * 32;
-        const uint4 w0 = ld_shared_v4(rsrc), w1 = ld_shared_v4(rsrc + 16);
-        const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-        const uint32_t bt = smem_u32(btile + sb * kMxB) + row * 128;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint2 lo = e2m1x8_to_e4m3x8(words[2 * j]);
-          const uint2 hi = e2m1x8_to_e4m3x8(words[2 * j + 1]);
-          const int c = 4 * half + j;
-          st_shared_v4(bt + ((c ^ (row & 7)) << 4), lo.x, lo.y, hi.x, hi.y);
-        }
-        const uint32_t sf_col = kMxSfCol0 + 8 * sb;
-        if (token_sf) {
-          // token row 32q + lane: lane 32q + lane, column sf_col + q
-          tmem_st1(lane_base + sf_col + q,
-                   ld_shared_u32(smem_u32(sfa + sa * 128 + q * 32 + lane)));
-        } else {
-          // weight row 32c + lane: lane (mod 32) of every quarter, column sf_col + 4 + c
-          const uint32_t* w = sfb + ws * kMxNT;
-          tmem_st4(lane_base + sf_col + 4, w[lane], w[32 + lane], w[64 + lane], w[96 + lane]);
-        }
-        tmem_st_wait();
-        fence_proxy_async_smem();  // generic-proxy tile writes -> tensor core reads
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&ready[sb]);
-          mbar_arrive(&wempty[ws]);
-        }
-      }
-    }
-  } else if (warp >= 12) {
+  } else {
     // ---------------- epilogue ----------------
     const int ew = warp & 3;
     const int row = ew * 32 + lane;
@@ -542,16 +468,25 @@ int launch_lowbit_gemm(int kind, const LowbitParams& p, int num_sms, cudaStream_
       return -1;
     attr_set = true;
   }
-  // packed weight codes [E*2F or E*H rows, K/2 bytes], box 64 bytes x 64 rows
+  // packed weight codes [E*2F or E*H rows, K codes], box 128 codes x 64 rows
   const int K = (kind == 0) ? p.H : p.F;
   const uint64_t rows = (kind == 0) ? static_cast<uint64_t>(p.E) * 2 * p.F
                                     : static_cast<uint64_t>(p.E) * p.H;
-  CUtensorMap tm_w;
-  if (!make_map_u8(&tm_w, p.w, rows, static_cast<uint64_t>(K) / 2, 64, 64)) return -1;
-  if (kind == 0)
-    lowbit_gemm_kernel<0><<<num_sms, kMxThreads, kMxSmem, stream>>>(tm_w, p);
-  else
-    lowbit_gemm_kernel<1><<<num_sms, kMxThreads, kMxSmem, stream>>>(tm_w, p);
+  // the same bytes as a plain byte map (box 64 bytes x 64 rows) for the L2 warm-up
+  CUtensorMap tm_w, tm_wpf, tm_a;
+  if (!make_map_e2m1(&tm_w, p.w, rows, static_cast<uint64_t>(K), 64)) return -1;
+  if (!make_map_u8(&tm_wpf, p.w, rows, static_cast<uint64_t>(K) / 2, 64, 64)) return -1;
+  if (kind == 0) {
+    tm_a = tm_w;  // unused: GEMM1 gathers its token rows
+    lowbit_gemm_kernel<0><<<num_sms, kMxThreads, kMxSmem, stream>>>(tm_w, tm_wpf, tm_a, p);
+  } else {
+    // intermediate codes [cap_rows, F], one box = the data rows of a block
+    const uint32_t bmr = static_cast<uint32_t>(p.BM < 128 ? p.BM : 128);
+    if (!make_map_u8_sw128(&tm_a, p.act, static_cast<uint64_t>(p.cap_rows),
+                           static_cast<uint64_t>(p.F), bmr))
+      return -1;
+    lowbit_gemm_kernel<1><<<num_sms, kMxThreads, kMxSmem, stream>>>(tm_w, tm_wpf, tm_a, p);
+  }
   return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 

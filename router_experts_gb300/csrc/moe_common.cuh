@@ -250,10 +250,13 @@ MOE_DEV void store_release_gpu(int* p, int v) {
 // Barrier over the CTAs of a cooperative launch (all co-resident).  bar[0]
 // counts arrivals and is reset by the last CTA, bar[1] is a generation that
 // the last CTA advances; both start at zero.  The wait is bounded: on expiry
-// it records kErrTimeout and returns (the caller's outputs are then invalid).
-MOE_DEV void grid_barrier(int* bar, int nctas, int* err) {
+// it records kErrTimeout and returns false to every thread of the CTA (the
+// caller must then skip whatever depends on the other CTAs).
+MOE_DEV bool grid_barrier(int* bar, int nctas, int* err) {
+  __shared__ int gb_ok;
   __syncthreads();
   if (threadIdx.x == 0) {
+    int ok = 1;
     const int gen = load_acquire_gpu(bar + 1);
     __threadfence();
     const int old = ticket_add_acq_rel(bar, 1);
@@ -265,14 +268,17 @@ MOE_DEV void grid_barrier(int* bar, int nctas, int* err) {
       while (load_acquire_gpu(bar + 1) == gen) {
         if (clock64() - t0 > kWaitLimitCycles) {
           raise_error(err, kErrTimeout);
+          ok = 0;
           break;
         }
         __nanosleep(64);
       }
     }
     __threadfence();
+    gb_ok = ok;
   }
   __syncthreads();
+  return gb_ok != 0;
 }
 
 // Order-preserving map of fp32 onto uint32 (for warp max/min reductions).

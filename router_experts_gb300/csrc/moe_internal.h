@@ -108,9 +108,22 @@ int device_num_sms();
 // box = 64 columns x box_rows rows, zero fill out of bounds.
 bool make_map_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
                    uint32_t box_rows);
-// 2-D byte tensor map of a row-major [rows, cols] byte matrix, no swizzle,
-// box = box_cols bytes x box_rows rows, zero fill out of bounds.
+// 2-D byte tensor map of a row-major [rows, cols] byte matrix: 128-byte
+// swizzle, box = 128 bytes x box_rows rows, zero fill out of bounds.
+bool make_map_u8_sw128(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
+                       uint32_t box_rows);
+// 2-D byte map of a row-major [rows, cols] byte matrix, no swizzle, box =
+// box_cols bytes x box_rows rows, zero fill out of bounds.
 bool make_map_u8(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
                  uint32_t box_cols, uint32_t box_rows);
+// 2-D map of a row-major [rows, cols] matrix of e2m1 codes packed two per
+// byte (low nibble first): each 16 codes land in shared memory as their 8
+// packed bytes followed by an 8-byte gap that the copy leaves untouched (the
+// operand layout of the block-scaled MMA for 4-bit types); 128-byte swizzle,
+// box = 128 codes x box_rows rows.  base must be 32-byte aligned and cols a
+// multiple of 128.  A load completes cols/2 * rows bytes of transactions
+// (the packed size), not the shared-memory footprint.
+bool make_map_e2m1(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
+                   uint32_t box_rows);
 
 }  // namespace moe
