@@ -12,32 +12,36 @@
 //
 // The products run on the block-scaled tensor-core MMA (tcgen05.mma
 // kind::mxf8f6f4, A = e4m3, B = e2m1, one UE8M0 scale per 32 values of each
-// operand row, fp32 accumulation in TMEM).  Nothing is converted on the SMs:
+// operand row, fp32 accumulation in TMEM).  Nothing is converted on the SMs,
+// and the one thread that issues the MMAs does little else per K step than
+// wait on one barrier, issue four MMAs and one commit (every tcgen05
+// instruction costs that thread tens of nanoseconds):
 //   B = 128 weight rows, loaded by TMA straight from the packed e2m1 codes
 //       with the 16 x 4-bit / 16-byte tensor-map type: each 16 codes land as
 //       their 8 packed bytes plus an 8-byte gap, the MMA's 4-bit operand
 //       layout (the copy counts the packed bytes in its transactions);
 //   A = 128 token rows of e4m3 codes: GEMM1 gathers them by sorted_ids with
-//       cp.async, GEMM2 reads its contiguous intermediate rows by TMA;
-//   scale words (4 K-blocks of one row) are copied into a [32][4]-word image
-//       per operand (word c of image row l = operand row 32c + l) and moved
-//       to TMEM by the MMA thread with tcgen05.cp 32x128b.warpx4, which puts
-//       image row l in lane l of every lane quarter: row m of A reads lane m,
-//       column base + m/32; row n of B reads lane n mod 32, column base + 4 +
-//       n/32; byte j of the word scales K-block j of the step.
+//       cp.async (the MMA thread fences the generic-proxy writes before the
+//       tensor core reads them); GEMM2 reads its contiguous intermediate rows
+//       with one 2-D TMA copy;
+//   scale words (4 K-blocks of one row) are written to TMEM by four warps,
+//       one per TMEM lane quarter, with tcgen05.st: row m of A at lane m,
+//       column base + m/32; row n of B at lane n mod 32 of every quarter,
+//       column base + 4 + n/32; byte j scales K-block j of the step.  The
+//       words are staged in groups of 4 steps (one 16-byte copy per row and
+//       operand) a few groups ahead.
 // Tile: M = 128 token rows of one block (BLOCK_M rows valid), N = 128 weight
 // rows (GEMM1: 64 gate rows + the matching 64 up rows), K steps of 128 (four
-// K = 32 MMAs).  Two 128-column accumulators, double-buffered; the scale
-// words of a step sit in an 8-column TMEM slot tied to its weight stage.
-// 10 warps:
+// K = 32 MMAs).  One ring of K steps (token tile + weight tile + an 8-column
+// TMEM scale slot) with one full and one empty barrier per step.  Two
+// 128-column accumulators, double-buffered.
+// 14 warps:
 //   warp 0      TMA of the weight tiles (L2 warmed kMxL2Ahead steps ahead
 //               through a plain byte map of the same codes)
-//               and, one row per lane, cp.async of their scale words
-//   warp 1      TMEM allocation and the single thread issuing tcgen05.cp and
-//               the MMAs
-//   warps 2-5   token tiles: GEMM1 cp.async gather of the codes and scale
-//               words; GEMM2 TMA of the codes, cp.async of the scale words
-//   warps 6-9   epilogue (TMEM lane quarter = warp % 4)
+//   warp 1      TMEM allocation and the single thread issuing the MMAs
+//   warps 2-5   token tiles (GEMM1 cp.async gather; GEMM2 one TMA copy)
+//   warps 6-9   scale words -> TMEM (lane quarter = warp % 4)
+//   warps 10-13 epilogue (lane quarter = warp % 4)
 #include <cuda_fp8.h>
 
 #include "moe_common.cuh"
@@ -47,22 +51,24 @@ namespace moe {
 
 namespace {
 
-constexpr int kMxThreads = 320;
+constexpr int kMxThreads = 448;
 constexpr int kMxBK = 128;                  // K values per stage (4 MMAs of K = 32)
 constexpr int kMxNT = 128;                  // weight rows per tile (MMA N)
-constexpr int kMxAStages = 7;               // token tiles
-constexpr int kMxBStages = 6;               // weight tiles (and TMEM scale slots)
+constexpr int kMxStages = 6;                // ring of K steps
 constexpr int kMxL2Ahead = 12;              // weight steps warmed in L2 ahead of their load
-constexpr int kMxTile = 128 * kMxBK;        // 16 KB per tile (one byte per code in smem)
-constexpr int kMxSfImg = 128 * 4;           // 512 B: one operand's scale words of a step
-constexpr int kMxBarBytes = 512;
-constexpr int kMxSmem =
-    (kMxAStages + kMxBStages) * (kMxTile + kMxSfImg) + kMxBarBytes + 1024;
+constexpr int kMxSfSlots = 3;               // scale staging slots, 4 K steps each
+constexpr int kMxTile = 128 * kMxBK;        // 16 KB per operand tile (one byte per code in smem)
+constexpr int kMxStageBytes = 2 * kMxTile;  // token tile + weight tile
+// scale staging: [kMxSfSlots][token | weight][128 rows][4 steps x 4 bytes]
+constexpr int kMxSfStageBytes = kMxSfSlots * 2 * 128 * 16;
+constexpr int kMxBarBytes = 256;
+constexpr int kMxSmem = kMxStages * kMxStageBytes + kMxSfStageBytes + kMxBarBytes + 1024;
 static_assert(kMxSmem <= 232448, "shared memory budget");
 constexpr uint32_t kMxAccCols = 128;        // per accumulator buffer
-constexpr uint32_t kMxSfCol0 = 256;         // scale slots: 8 columns per weight stage
+constexpr uint32_t kMxSfCol0 = 256;         // scale slots: 8 columns per ring stage
 constexpr uint32_t kMxTmemCols = 512;
-static_assert(kMxSfCol0 + 8 * kMxBStages <= kMxTmemCols, "TMEM columns");
+static_assert(kMxSfCol0 + 8 * kMxStages <= kMxTmemCols, "TMEM columns");
+static_assert(2 * (kMxStages + 2) * 8 + 8 <= kMxBarBytes, "barrier space");
 
 // Instruction descriptor of the block-scaled MMA: e4m3 A, e2m1 B (both
 // K-major), UE8M0 scales, fp32 D; sf_id picks the scale byte of the 32-bit
@@ -84,23 +90,20 @@ MOE_DEV void umma_mxf8f4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint
       : "memory");
 }
 
-// Shared-memory descriptor of a [32 rows x 16 bytes] image, no swizzle: one
-// 16-byte core-matrix column, row groups of 8 every 128 bytes.
-MOE_DEV uint64_t sf_image_desc(uint32_t smem_byte_addr) {
-  uint64_t d = 0;
-  d |= static_cast<uint64_t>((smem_byte_addr & 0x3FFFFu) >> 4);  // start address
-  d |= static_cast<uint64_t>(1) << 16;                           // leading byte offset (unused)
-  d |= static_cast<uint64_t>(128 >> 4) << 32;                    // stride byte offset
-  d |= static_cast<uint64_t>(1) << 46;                           // descriptor version
-  return d;
+// Warp-wide TMEM stores (lane i of the warp -> TMEM lane (address lane field + i)).
+MOE_DEV void tmem_st1(uint32_t taddr, uint32_t v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
 }
-
-// Copy a [32 x 128-bit] shared-memory image into 4 TMEM columns of every lane
-// quarter (image row l -> lanes l, 32 + l, 64 + l, 96 + l).  Ordered before
-// the MMAs the same thread issues after it.
-MOE_DEV void tmem_cp_32x128_x4(uint32_t taddr, uint64_t desc) {
-  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc)
+MOE_DEV void tmem_st4(uint32_t taddr, uint32_t v0, uint32_t v1, uint32_t v2, uint32_t v3) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr),
+               "r"(v0), "r"(v1), "r"(v2), "r"(v3)
                : "memory");
+}
+MOE_DEV void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+MOE_DEV uint32_t ld_shared_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
 }
 
 // e4m3 codes of 32 activations with their UE8M0 exponent byte: scale = the
@@ -155,15 +158,11 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  uint8_t* atile = smem;                              // [kMxAStages][128 rows x 128 codes]
-  uint8_t* btile = atile + kMxAStages * kMxTile;      // [kMxBStages][128 rows x 128 slots]
-  uint32_t* sfa = reinterpret_cast<uint32_t*>(btile + kMxBStages * kMxTile);  // [kMxAStages][128]
-  uint32_t* sfb = sfa + kMxAStages * 128;                                     // [kMxBStages][128]
-  uint64_t* afull = reinterpret_cast<uint64_t*>(sfb + kMxBStages * 128);
-  uint64_t* aempty = afull + kMxAStages;
-  uint64_t* bfull = aempty + kMxAStages;
-  uint64_t* bempty = bfull + kMxBStages;
-  uint64_t* tfull = bempty + kMxBStages;
+  // ring stage s: token tile at s * kMxStageBytes, weight tile kMxTile after it
+  uint32_t* sfstage = reinterpret_cast<uint32_t*>(smem + kMxStages * kMxStageBytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kMxStages * kMxStageBytes + kMxSfStageBytes);
+  uint64_t* empty = full + kMxStages;
+  uint64_t* tfull = empty + kMxStages;
   uint64_t* tempty = tfull + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -179,14 +178,11 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   const int bmr = min(p.BM, 128);  // token rows of a tile that hold data
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kMxAStages; ++i) {
-      // gather threads (cp.async arrivals); GEMM2 adds the TMA's expect-tx arrival
-      mbar_init(&afull[i], 128 + (KIND == 1 ? 1 : 0));
-      mbar_init(&aempty[i], 1);  // MMA commit
-    }
-    for (int i = 0; i < kMxBStages; ++i) {
-      mbar_init(&bfull[i], 1 + 32);  // TMA bytes + the scale-word copies of warp 0
-      mbar_init(&bempty[i], 1);      // MMA commit
+    for (int i = 0; i < kMxStages; ++i) {
+      // weight TMA expect-tx arrival + tokens (GEMM1: 128 cp.async arrivals,
+      // GEMM2: one TMA expect-tx arrival) + the four scale warps
+      mbar_init(&full[i], 1 + (KIND == 0 ? 128 : 1) + 4);
+      mbar_init(&empty[i], 1);  // MMA commit
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&tfull[i], 1);
@@ -213,30 +209,28 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     u.e = e;
     return u;
   };
+  // token row of tile row r (GEMM1), or -1 for a padding row
+  auto token_of = [&](const MxUnit& u, int r) -> int {
+    if (r >= p.BM) return -1;
+    const int a = __ldg(p.sorted_ids + static_cast<size_t>(u.b) * p.BM + r);
+    return (a >= 0 && a < p.T * p.k) ? a / p.k : -1;
+  };
 
   if (warp == 0) {
-    // ---------------- weight tiles (TMA) + their scale words ----------------
+    // ---------------- weight tiles (TMA) ----------------
     if (lane == 0) {
       tma_prefetch_desc(&tm_w);
       tma_prefetch_desc(&tm_wpf);
-    }
-    uint32_t it = 0;
-    bool alive = true;
-    for (int uu = blockIdx.x; alive && uu < num_units; uu += gridDim.x) {
-      const MxUnit u = decode(uu);
-      // lane l copies the scale words of rows l, 32 + l, 64 + l, 96 + l: image
-      // row l, words 0..3
-      const uint8_t* srow[4];
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-        srow[c] = p.w_scale + static_cast<size_t>(mx_wrow<KIND>(p, u, lane + 32 * c)) * (K / 32);
-      const int r0 = mx_wrow<KIND>(p, u, 0), r64 = mx_wrow<KIND>(p, u, 64);
-      // the next unit of this CTA, for warming L2 across the unit boundary
-      const bool has_next = uu + static_cast<int>(gridDim.x) < num_units;
-      const MxUnit nu = has_next ? decode(uu + gridDim.x) : u;
-      const int n0 = mx_wrow<KIND>(p, nu, 0), n64 = mx_wrow<KIND>(p, nu, 64);
-      for (int ks = 0; ks < KS; ++ks, ++it) {
-        if (lane == 0) {
+      uint32_t it = 0;
+      bool alive = true;
+      for (int uu = blockIdx.x; alive && uu < num_units; uu += gridDim.x) {
+        const MxUnit u = decode(uu);
+        const int r0 = mx_wrow<KIND>(p, u, 0), r64 = mx_wrow<KIND>(p, u, 64);
+        // the next unit of this CTA, for warming L2 across the unit boundary
+        const bool has_next = uu + static_cast<int>(gridDim.x) < num_units;
+        const MxUnit nu = has_next ? decode(uu + gridDim.x) : u;
+        const int n0 = mx_wrow<KIND>(p, nu, 0), n64 = mx_wrow<KIND>(p, nu, 64);
+        for (int ks = 0; ks < KS; ++ks, ++it) {
           int pk = ks + kMxL2Ahead, p0 = r0, p64 = r64;
           if (pk >= KS && has_next) {
             pk -= KS;
@@ -247,28 +241,19 @@ __global__ void __launch_bounds__(kMxThreads, 1)
             tma_prefetch_l2_2d(&tm_wpf, pk * (kMxBK / 2), p0);
             tma_prefetch_l2_2d(&tm_wpf, pk * (kMxBK / 2), p64);
           }
-        }
-        const int ws = it % kMxBStages;
-        const uint32_t ph = (it / kMxBStages) & 1u;
-        const bool ok = mbar_wait(&bempty[ws], ph ^ 1u, abort_flag, p.err);
-        if (__any_sync(0xffffffffu, !ok)) {
-          alive = false;
-          break;
-        }
-        if (lane == 0) {
-          uint8_t* dst = btile + ws * kMxTile;
+          const int s = it % kMxStages;
+          if (!mbar_wait(&empty[s], ((it / kMxStages) & 1u) ^ 1u, abort_flag, p.err)) {
+            alive = false;
+            break;
+          }
+          uint8_t* dst = smem + s * kMxStageBytes + kMxTile;
           // two 64-row boxes of 128 codes: 2 x 64 x 64 packed bytes
-          mbar_arrive_expect_tx(&bfull[ws], kMxNT * kMxBK / 2);
-          tma_load_2d(dst, &tm_w, &bfull[ws], ks * kMxBK, r0);
-          tma_load_2d(dst + 64 * 128, &tm_w, &bfull[ws], ks * kMxBK, r64);
+          mbar_arrive_expect_tx(&full[s], kMxNT * kMxBK / 2);
+          tma_load_2d(dst, &tm_w, &full[s], ks * kMxBK, r0);
+          tma_load_2d(dst + 64 * 128, &tm_w, &full[s], ks * kMxBK, r64);
         }
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-          cp_async_4(smem_u32(sfb + ws * 128 + 4 * lane + c), srow[c] + ks * 4, 4u);
-        cp_async_mbar_arrive_noinc(&bfull[ws]);
       }
     }
-    cp_async_wait_all();
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
@@ -276,107 +261,177 @@ __global__ void __launch_bounds__(kMxThreads, 1)
       bool alive = true;
       for (int uu = blockIdx.x; alive && uu < num_units; uu += gridDim.x, ++acc_it) {
         const int buf = acc_it & 1;
-        const uint32_t aph = (acc_it >> 1) & 1u;
-        if (!mbar_wait(&tempty[buf], aph ^ 1u, abort_flag, p.err)) break;
+        if (!mbar_wait(&tempty[buf], ((acc_it >> 1) & 1u) ^ 1u, abort_flag, p.err)) break;
         tc_fence_after();
         const uint32_t d = tmem_base + buf * kMxAccCols;
         for (int ks = 0; ks < KS; ++ks, ++it) {
-          const int sa = it % kMxAStages, sb = it % kMxBStages;
-          if (!mbar_wait(&afull[sa], (it / kMxAStages) & 1u, abort_flag, p.err) ||
-              !mbar_wait(&bfull[sb], (it / kMxBStages) & 1u, abort_flag, p.err)) {
+          const int s = it % kMxStages;
+          if (!mbar_wait(&full[s], (it / kMxStages) & 1u, abort_flag, p.err)) {
             alive = false;
             break;
           }
-          fence_proxy_async_smem();  // cp.async rows and scale words -> tensor core
+          if constexpr (KIND == 0) fence_proxy_async_smem();  // cp.async rows -> tensor core
           tc_fence_after();
-          // The scale slot of weight stage sb was last read by the MMAs of step
-          // it - kMxBStages, complete before that stage was refilled.
-          const uint32_t sf_t = tmem_base + kMxSfCol0 + 8 * sb;
-          tmem_cp_32x128_x4(sf_t, sf_image_desc(smem_u32(sfa + sa * 128)));
-          tmem_cp_32x128_x4(sf_t + 4, sf_image_desc(smem_u32(sfb + sb * 128)));
-          const uint32_t a_addr = smem_u32(atile + sa * kMxTile);
-          const uint32_t b_addr = smem_u32(btile + sb * kMxTile);
+          const uint32_t a_addr = smem_u32(smem + s * kMxStageBytes);
+          const uint32_t b_addr = a_addr + kMxTile;
+          const uint32_t sf_t = tmem_base + kMxSfCol0 + 8 * s;
 #pragma unroll
           for (int kk = 0; kk < kMxBK / 32; ++kk)
             umma_mxf8f4(d, sw128_desc(a_addr + kk * 32), sw128_desc(b_addr + kk * 32),
                         idesc_mxf8f4(128, kMxNT, kk), sf_t, sf_t + 4,
                         (ks > 0 || kk > 0) ? 1u : 0u);
-          umma_commit(&aempty[sa]);
-          umma_commit(&bempty[sb]);
+          umma_commit(&empty[s]);
         }
         if (!alive) break;
         umma_commit(&tfull[buf]);
       }
     }
   } else if (warp < 6) {
-    // ---------------- token tiles + their scale words ----------------
-    const int gt = threadIdx.x - 64;  // 0..127
-    const int chunk = gt & 7;
-    // image slot of row gt's scale word: image row gt % 32, word gt / 32
-    const int sf_word = 4 * (gt & 31) + (gt >> 5);
-    uint32_t it = 0;
-    bool alive = true;
-    auto row_src = [&](const MxUnit& u, int r, const uint8_t*& codes, const uint8_t*& scales) {
-      codes = nullptr;
-      scales = nullptr;
-      if (r >= p.BM) return;
-      const size_t prow = static_cast<size_t>(u.b) * p.BM + r;
-      if constexpr (KIND == 0) {
-        const int a = __ldg(p.sorted_ids + prow);
-        if (a < 0 || a >= p.T * p.k) return;
-        const size_t tok = static_cast<size_t>(a / p.k);
-        codes = p.act + tok * K;
-        scales = p.act_scale + tok * (K / 32);
-      } else {
-        codes = p.act + prow * K;
-        scales = p.act_scale + prow * (K / 32);
-      }
-    };
-    if (KIND == 1 && gt == 0) tma_prefetch_desc(&tm_a);
-    for (int uu = blockIdx.x; alive && uu < num_units; uu += gridDim.x) {
-      const MxUnit u = decode(uu);
-      const uint8_t* src[8];
-      const uint8_t* ssrc;
-      {
-        const uint8_t* cd;
-        row_src(u, gt, cd, ssrc);
-      }
-      if constexpr (KIND == 0) {
+    // ---------------- token tiles ----------------
+    if constexpr (KIND == 0) {
+      // cp.async gather: thread gt copies 16-byte chunk gt % 8 of tile rows
+      // gt/8 + 16i; its arrival counts when its copies have landed (the MMA
+      // thread fences before the tensor core reads them)
+      const int gt = threadIdx.x - 64;  // 0..127
+      const int chunk = gt & 7;
+      uint32_t it = 0;
+      bool alive = true;
+      for (int uu = blockIdx.x; alive && uu < num_units; uu += gridDim.x) {
+        const MxUnit u = decode(uu);
+        const uint8_t* src[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const uint8_t* sc;
-          row_src(u, (gt >> 3) + 16 * i, src[i], sc);
+          const int tr = token_of(u, (gt >> 3) + 16 * i);
+          src[i] = tr >= 0 ? p.act + static_cast<size_t>(tr) * K + chunk * 16 : nullptr;
         }
-      }
-      for (int ks = 0; ks < KS; ++ks, ++it) {
-        const int s = it % kMxAStages;
-        const uint32_t ph = (it / kMxAStages) & 1u;
-        if (!mbar_wait(&aempty[s], ph ^ 1u, abort_flag, p.err)) {
-          alive = false;
-          break;
-        }
-        if constexpr (KIND == 0) {
-          const uint32_t tile = smem_u32(atile + s * kMxTile);
+        for (int ks = 0; ks < KS; ++ks, ++it) {
+          const int s = it % kMxStages;
+          if (!mbar_wait(&empty[s], ((it / kMxStages) & 1u) ^ 1u, abort_flag, p.err)) {
+            alive = false;
+            break;
+          }
+          const uint32_t tile = smem_u32(smem + s * kMxStageBytes);
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             const int r = (gt >> 3) + 16 * i;
-            const uint32_t dst = tile + r * 128 + ((chunk ^ (r & 7)) << 4);
-            cp_async_16(dst,
-                        src[i] ? static_cast<const void*>(src[i] + ks * kMxBK + chunk * 16) : p.act,
+            cp_async_16(tile + r * 128 + ((chunk ^ (r & 7)) << 4),
+                        src[i] ? static_cast<const void*>(src[i] + ks * kMxBK) : p.act,
                         src[i] ? 16u : 0u);
           }
-        } else {
-          // the block's rows are contiguous: one box of bmr rows
-          if (gt == 0) {
-            mbar_arrive_expect_tx(&afull[s], static_cast<uint32_t>(bmr) * kMxBK);
-            tma_load_2d(atile + s * kMxTile, &tm_a, &afull[s], ks * kMxBK, u.b * p.BM);
-          }
+          cp_async_mbar_arrive_noinc(&full[s]);
         }
-        cp_async_4(smem_u32(sfa + s * 128 + sf_word),
-                   ssrc ? static_cast<const void*>(ssrc + ks * 4) : p.act_scale, ssrc ? 4u : 0u);
-        // the stage barrier counts this thread's arrival when its copies land
-        cp_async_mbar_arrive_noinc(&afull[s]);
       }
+      cp_async_wait_all();
+    } else if (warp == 2 && lane == 0) {
+      // the block's rows are contiguous: one 2-D box of bmr rows per step
+      tma_prefetch_desc(&tm_a);
+      uint32_t it = 0;
+      bool alive = true;
+      for (int uu = blockIdx.x; alive && uu < num_units; uu += gridDim.x) {
+        const MxUnit u = decode(uu);
+        for (int ks = 0; ks < KS; ++ks, ++it) {
+          const int s = it % kMxStages;
+          if (!mbar_wait(&empty[s], ((it / kMxStages) & 1u) ^ 1u, abort_flag, p.err)) {
+            alive = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(bmr) * kMxBK);
+          tma_load_2d(smem + s * kMxStageBytes, &tm_a, &full[s], ks * kMxBK, u.b * p.BM);
+        }
+      }
+    }
+  } else if (warp < 10) {
+    // ---------------- scale words -> TMEM ----------------
+    // The four warps (lane quarter q = warp % 4) stage the scale words of
+    // groups of 4 K steps in a ring of kMxSfSlots slots; thread (q, l) copies
+    // those of token row 32q + l and of weight row 32q + l (16 bytes = 4 steps
+    // when a scale row is a multiple of 16 bytes, else one word per step),
+    // kMxSfSlots - 1 groups ahead.  After a named barrier of the four warps
+    // every thread reads the word of its token row and the words of weight
+    // rows l, 32 + l, 64 + l, 96 + l, and stores them into the step's TMEM
+    // slot once the MMAs that last read that slot are done.
+    const int q = warp & 3;
+    const int r = 32 * q + lane;  // staged row of this thread
+    const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+    const uint32_t stage_base = smem_u32(sfstage);  // [slot][A | B][128 rows][16 bytes]
+    const int my_units = num_units > static_cast<int>(blockIdx.x)
+                             ? (num_units - static_cast<int>(blockIdx.x) + gridDim.x - 1) / gridDim.x
+                             : 0;
+    const int gpu = (KS + 3) / 4;  // groups per unit
+    const int n_g = my_units * gpu;
+    // 16-byte copies need 16-byte aligned scale rows (row length and base)
+    const bool wide = (K / 32) % 16 == 0 &&
+                      (reinterpret_cast<uintptr_t>(p.act_scale) & 15u) == 0 &&
+                      (reinterpret_cast<uintptr_t>(p.w_scale) & 15u) == 0;
+    int pf_unit = -1;
+    const uint8_t* pa = nullptr;
+    const uint8_t* pb = nullptr;
+    auto issue = [&](int g) {
+      const int un = g / gpu, gi = g % gpu;
+      if (un != pf_unit) {
+        pf_unit = un;
+        const MxUnit u = decode(static_cast<int>(blockIdx.x) + un * static_cast<int>(gridDim.x));
+        pa = nullptr;
+        if constexpr (KIND == 0) {
+          const int t = token_of(u, r);
+          if (t >= 0) pa = p.act_scale + static_cast<size_t>(t) * (K / 32);
+        } else {
+          if (r < p.BM) pa = p.act_scale + (static_cast<size_t>(u.b) * p.BM + r) * (K / 32);
+        }
+        pb = p.w_scale + static_cast<size_t>(mx_wrow<KIND>(p, u, r)) * (K / 32);
+      }
+      const uint32_t dst = stage_base + (g % kMxSfSlots) * 4096 + r * 16;
+      if (wide) {
+        cp_async_16(dst, pa ? static_cast<const void*>(pa + 16 * gi) : p.act_scale, pa ? 16u : 0u);
+        cp_async_16(dst + 2048, pb + 16 * gi, 16u);
+      } else {
+        const int nw = min(4, KS - 4 * gi);
+        for (int w = 0; w < nw; ++w) {
+          cp_async_4(dst + 4 * w, pa ? static_cast<const void*>(pa + 16 * gi + 4 * w) : p.act_scale,
+                     pa ? 4u : 0u);
+          cp_async_4(dst + 2048 + 4 * w, pb + 16 * gi + 4 * w, 4u);
+        }
+      }
+    };
+    for (int g = 0; g < kMxSfSlots - 1; ++g) {
+      if (g < n_g) issue(g);
+      cp_async_commit();
+    }
+    bool alive = true;
+    for (int g = 0; alive && g < n_g; ++g) {
+      cp_async_wait<kMxSfSlots - 2>();  // this thread's copies of group g have landed
+      // every thread's copies of group g have landed, and every thread has
+      // read group g - 1, whose slot the next copies reuse
+      named_bar_sync(2, 128);
+      if (g + kMxSfSlots - 1 < n_g) issue(g + kMxSfSlots - 1);
+      cp_async_commit();  // one group per iteration (empty past the end)
+      const uint32_t slot = stage_base + (g % kMxSfSlots) * 4096;
+      const int gi = g % gpu;
+      const int j0 = (g / gpu) * KS + 4 * gi;
+      const int nst = min(4, KS - 4 * gi);
+      for (int t = 0; t < nst; ++t) {
+        const uint32_t wa = ld_shared_u32(slot + r * 16 + 4 * t);
+        uint32_t wb[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) wb[c] = ld_shared_u32(slot + 2048 + (32 * c + lane) * 16 + 4 * t);
+        const int j = j0 + t;
+        const int s = j % kMxStages;
+        // the slot's previous scales were read by the MMAs of step j - kMxStages
+        const bool ok = mbar_wait(&empty[s], ((j / kMxStages) & 1u) ^ 1u, abort_flag, p.err);
+        if (__any_sync(0xffffffffu, !ok)) {
+          alive = false;
+          break;
+        }
+        const uint32_t col = kMxSfCol0 + 8 * s;
+        tmem_st1(lane_base + col + q, wa);
+        tmem_st4(lane_base + col + 4, wb[0], wb[1], wb[2], wb[3]);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&full[s]);
+      }
+      // the four warps stop together (they meet at the named barrier)
+      if (named_bar_any(3, 128, !alive)) alive = false;
     }
     cp_async_wait_all();
   } else {
@@ -468,16 +523,16 @@ int launch_lowbit_gemm(int kind, const LowbitParams& p, int num_sms, cudaStream_
       return -1;
     attr_set = true;
   }
-  // packed weight codes [E*2F or E*H rows, K codes], box 128 codes x 64 rows
+  // packed weight codes [E*2F or E*H rows, K codes], box 128 codes x 64 rows;
+  // the same bytes as a plain byte map (box 64 bytes x 64 rows) for the L2 warm-up
   const int K = (kind == 0) ? p.H : p.F;
   const uint64_t rows = (kind == 0) ? static_cast<uint64_t>(p.E) * 2 * p.F
                                     : static_cast<uint64_t>(p.E) * p.H;
-  // the same bytes as a plain byte map (box 64 bytes x 64 rows) for the L2 warm-up
   CUtensorMap tm_w, tm_wpf, tm_a;
   if (!make_map_e2m1(&tm_w, p.w, rows, static_cast<uint64_t>(K), 64)) return -1;
   if (!make_map_u8(&tm_wpf, p.w, rows, static_cast<uint64_t>(K) / 2, 64, 64)) return -1;
   if (kind == 0) {
-    tm_a = tm_w;  // unused: GEMM1 gathers its token rows
+    tm_a = tm_w;  // unused: GEMM1 gathers its token rows with cp.async
     lowbit_gemm_kernel<0><<<num_sms, kMxThreads, kMxSmem, stream>>>(tm_w, tm_wpf, tm_a, p);
   } else {
     // intermediate codes [cap_rows, F], one box = the data rows of a block

@@ -105,14 +105,31 @@ def test_lowbit_layer_matches_oracle(T, ntok):
     assert err <= LAYER_RTOL_LOWBIT
 
 
+def _shifted(t, off):
+    """A copy of t whose data starts `off` bytes past a 16-byte boundary."""
+    flat = t.reshape(-1)
+    buf = torch.empty(flat.numel() + 16, dtype=t.dtype, device=t.device)
+    view = buf[off:off + flat.numel()]
+    view.copy_(flat)
+    return view.view(t.shape)
+
+
 # Small low-bit shapes: one 64-feature GEMM1 tile and one 128-column GEMM2 tile
-# (H = 128, F = 128), several tiles with a ragged last block, BLOCK_M 16/64/128.
-@pytest.mark.parametrize("T,E,k,H,F,BM", [(5, 8, 2, 128, 128, 16), (40, 8, 2, 256, 128, 16),
-                                          (300, 16, 4, 256, 256, 64),
-                                          (700, 8, 2, 384, 128, 128)])
-def test_lowbit_small_shapes(T, E, k, H, F, BM):
+# (H = 128, F = 128), several tiles with a ragged last block, BLOCK_M 16/64/128;
+# scale rows of 16 bytes (H = F = 512: one group of 4 K steps copied whole) and
+# the same with the scale arrays 4 bytes off a 16-byte boundary (word copies).
+@pytest.mark.parametrize("T,E,k,H,F,BM,off", [(5, 8, 2, 128, 128, 16, 0),
+                                              (40, 8, 2, 256, 128, 16, 0),
+                                              (300, 16, 4, 256, 256, 64, 0),
+                                              (700, 8, 2, 384, 128, 128, 0),
+                                              (200, 8, 2, 512, 512, 64, 0),
+                                              (200, 8, 2, 512, 512, 64, 4)])
+def test_lowbit_small_shapes(T, E, k, H, F, BM, off):
     w = W.Workload("lb", H=H, E=E, k=k, F=F, scoring="sigmoid", bias=True, lowbit=True)
     d = W.make_inputs(w, T, seed=T, device="cuda")
+    if off:
+        for key in ("hidden_scale", "w13_scale", "w2_scale"):
+            d[key] = _shifted(d[key], off)
     ids, wts = W.random_routing(T, k, E, seed=T)
     s, b, n = moe.align(ids.cuda(), E, BM)
     out = moe.grouped_ffn(d["hidden"], d["w13"], d["w2"], k, BM, s, b, n, wts.cuda(),
@@ -123,5 +140,5 @@ def test_lowbit_small_shapes(T, E, k, H, F, BM):
     tokens = np.arange(T, dtype=np.int32)
     ref = oracle_ffn_lowbit(d, tokens, ids.numpy(), wts.numpy(), w)
     err = rel_err(y.float().cpu().numpy(), ref)
-    print(f"low-bit T={T} E={E} k={k} H={H} F={F} BM={BM}: rel err {err:.2e}")
+    print(f"low-bit T={T} E={E} k={k} H={H} F={F} BM={BM} scale offset {off}: rel err {err:.2e}")
     assert err <= LAYER_RTOL_LOWBIT
