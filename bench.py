@@ -587,8 +587,8 @@ def run_ours(args):
         "stage_note": "each kernel as its own graph, %d replays with events between them" % Ks,
         "sweep": sweep,
         "e2e": e2e,
-        "gpu_launches": K * (len(names) - 1 + moe.router_kernel_count(
-            T, H, E, "e4m3" if w.lowbit else "bf16", "f32" if w.lowbit else "bf16")),
+        "gpu_launches": K * moe.layer_kernel_count(
+            T, H, F, E, k, "e4m3" if w.lowbit else "bf16", "f32" if w.lowbit else "bf16"),
         "cpu_baseline": cpu,
         "device_error_word": code,
     }

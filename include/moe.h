@@ -237,8 +237,11 @@ int moe_finalize(const void* stage, int T, int k, int H, void* out, void* stream
  * else 128 ([P3] "Tile shape is the main tuning knob ... depends on tokens
  * per expert").  act_dt/w_dt as for the expert GEMMs; the router reads
  * `hidden` (dequantised when E4M3).  out [T,H] bf16.
+ * moe_layer_kernel_count returns how many kernels moe_layer enqueues for
+ * these shapes and types (0 when T == 0 or the arguments are invalid).
  * ------------------------------------------------------------------------- */
 size_t moe_layer_workspace_bytes(int T, int H, int F, int E, int k, int block_m, int act_dt);
+int moe_layer_kernel_count(int T, int H, int F, int E, int k, int act_dt, int gate_dt);
 int moe_layer(const void* hidden, int act_dt, const uint8_t* hidden_scale, const void* gate,
               int gate_dt, const float* bias, const void* w13, const uint8_t* w13_scale,
               const void* w2, const uint8_t* w2_scale, int w_dt, int T, int H, int F, int E,

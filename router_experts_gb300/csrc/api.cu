@@ -446,6 +446,12 @@ size_t moe_layer_workspace_bytes(int T, int H, int F, int E, int k, int block_m,
   return layer_layout(T, H, F, E, k, block_m, act_dt).total;
 }
 
+int moe_layer_kernel_count(int T, int H, int F, int E, int k, int act_dt, int gate_dt) {
+  if (T <= 0 || H <= 0 || F <= 0 || E <= 0 || k <= 0) return 0;
+  // router + align, GEMM1, GEMM2, finalize
+  return moe_router_kernel_count(T, H, E, act_dt, gate_dt) + 4;
+}
+
 int moe_layer(const void* hidden, int act_dt, const uint8_t* hidden_scale, const void* gate,
               int gate_dt, const float* bias, const void* w13, const uint8_t* w13_scale,
               const void* w2, const uint8_t* w2_scale, int w_dt, int T, int H, int F, int E,

@@ -48,6 +48,7 @@ def load():
         sig = {
             "moe_router_workspace_bytes": (SZ, [I, I, I]),
             "moe_router_kernel_count": (I, [I, I, I, I, I]),
+            "moe_layer_kernel_count": (I, [I, I, I, I, I, I, I]),
             "moe_router": (I, [P, I, P, P, I, P, I, I, I, I, I, I, I, I, F, P, P, P, SZ, P]),
             "moe_align_workspace_bytes": (SZ, []),
             "moe_align": (I, [P, I, I, I, I, P, I64, P, P, P, SZ, P]),
@@ -142,6 +143,13 @@ def router_kernel_count(T: int, H: int, E: int, hidden_dtype="bf16", gate_dtype=
     """Kernels moe_router enqueues for these shapes and types."""
     dt = {"bf16": DT_BF16, "f32": DT_F32, "e4m3": DT_E4M3}
     return int(load().moe_router_kernel_count(T, H, E, dt[hidden_dtype], dt[gate_dtype]))
+
+
+def layer_kernel_count(T: int, H: int, F: int, E: int, k: int, act_dtype="bf16",
+                       gate_dtype="bf16") -> int:
+    """Kernels moe_layer enqueues for these shapes and types."""
+    dt = {"bf16": DT_BF16, "f32": DT_F32, "e4m3": DT_E4M3}
+    return int(load().moe_layer_kernel_count(T, H, F, E, k, dt[act_dtype], dt[gate_dtype]))
 
 
 # ---- entry points ---------------------------------------------------------------

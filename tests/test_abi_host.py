@@ -112,3 +112,17 @@ def test_align_and_ffn_reject_bad_arguments(lib):
     assert rc == 2
     assert lib.moe_finalize(P(4096), 4, 2, 60, P(4096), None) == 1  # H % 8
     assert lib.moe_finalize(P(4096), 0, 2, 64, P(4096), None) == 0  # T = 0
+
+
+def test_layer_kernel_count(lib):
+    # router launches (two for bf16 hidden and gate; one below 8 tokens for an
+    # fp32 gate; conversion + GEMM + selection for e4m3 hidden with an fp32
+    # gate; one for more experts than the tensor-core router covers), then
+    # align, GEMM1, GEMM2 and finalize
+    assert lib.moe_layer_kernel_count(1, 2048, 768, 128, 8, 0, 0) == 6
+    assert lib.moe_layer_kernel_count(4096, 2048, 768, 128, 8, 0, 0) == 6
+    assert lib.moe_layer_kernel_count(1, 4096, 2048, 256, 6, 2, 1) == 5
+    assert lib.moe_layer_kernel_count(8, 4096, 2048, 256, 6, 2, 1) == 7
+    assert lib.moe_layer_kernel_count(4096, 4096, 2048, 256, 6, 2, 1) == 7
+    assert lib.moe_layer_kernel_count(1, 2048, 768, 640, 8, 0, 0) == 5
+    assert lib.moe_layer_kernel_count(0, 2048, 768, 128, 8, 0, 0) == 0

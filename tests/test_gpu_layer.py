@@ -62,3 +62,26 @@ def test_layer_is_deterministic():
     assert torch.equal(a, b)
     ws = moe.default_workspace("cuda")
     assert moe.read_device_error(ws.buf) == 0
+
+
+# The layer must equal the separate public calls (router, align, grouped FFN,
+# finalize) bit for bit, across the align kernel's one-CTA / many-CTA switch
+# at T*k = 2048.
+@pytest.mark.parametrize("name,T", [("qwen3", 1), ("qwen3", 255), ("qwen3", 256),
+                                    ("qwen3", 257), ("dsv3", 256)])
+def test_layer_equals_separate_calls(name, T):
+    w = W.WORKLOADS[name]
+    d = W.make_inputs(w, T, seed=11, device="cuda")
+    bm = moe.pick_block_m(T, w.k, w.E)
+    y = moe.layer(d["hidden"], d["gate"], d.get("bias"), d["w13"], d["w2"], w.k, w.scoring,
+                  w.n_group, w.topk_group, w.renormalize, w.scaling)
+    ids, wts = moe.router(d["hidden"], d["gate"], d.get("bias"), w.k, w.scoring, w.n_group,
+                          w.topk_group, w.renormalize, w.scaling)
+    s, b, n = moe.align(ids, w.E, bm)
+    st = moe.grouped_ffn(d["hidden"], d["w13"], d["w2"], w.k, bm, s, b, n, wts)
+    y2 = moe.finalize(st, T, w.k)
+    torch.cuda.synchronize()
+    print(f"layer {name} T={T}: equal to the separate calls")
+    assert moe.layer_kernel_count(T, w.H, w.F, w.E, w.k) == 6
+    assert torch.equal(y, y2)
+    assert moe.read_device_error(moe.default_workspace("cuda").buf) == 0
