@@ -363,10 +363,14 @@ def run_ours(args):
     graphs, facts, keep_alive = stage_graphs(d["hidden"], d.get("hidden_scale"))
     BM, touched = facts["block_m"], facts["touched"]
 
-    weights_bytes = (d["w13"].numel() + d["w2"].numel()) * d["w13"].element_size()
+    # the bytes a step reads are the touched experts' weights (plus scales), not
+    # the whole weight tensors: only inputs larger than L2 make a flush needless
+    weights_bytes = ((d["w13"].numel() + d["w2"].numel()) * d["w13"].element_size()
+                     + sum(d[s].numel() for s in ("w13_scale", "w2_scale") if s in d))
+    weights_bytes = weights_bytes * touched // E
     lbk = dict(hidden_scale=d.get("hidden_scale"), w13_scale=d.get("w13_scale"),
                w2_scale=d.get("w2_scale")) if w.lowbit else {}
-    l2_note = ("inputs larger than L2 (expert weights %.2f GB)" % (weights_bytes / 1e9)
+    l2_note = ("inputs larger than L2 (weights of the touched experts %.2f GB)" % (weights_bytes / 1e9)
                if weights_bytes > 256e6 else "L2 flushed between steps (512 MB write, then 256 MB read)")
     flush = None if weights_bytes > 256e6 else L2Flush(torch, dev)
 

@@ -24,7 +24,9 @@
 //      leader advances the running base.  Positions are disjoint across CTAs.
 //   4. Fill: the pads of every expert, the tail up to the capacity, and the
 //      block table are split over all warps of the grid.
-// With G = 1 (small T*k) step 2 reads the CTA's own counts and skips the barrier.
+// With G = 1 (small T*k) step 2 reads the CTA's own counts and skips the
+// barrier; with at most 32 assignments one warp does the counting and placing
+// (align_few).
 #include "moe_common.cuh"
 #include "moe_internal.h"
 
@@ -76,6 +78,74 @@ MOE_DEV int load_id(const int32_t* __restrict__ ids, int a, int E) {
   return (v >= 0 && v < E) ? v : -1;
 }
 
+// Few assignments (n <= 32, decode): warp 0 handles them all with warp
+// intrinsics -- the lanes with the same expert (one ballot per id bit), each
+// group's start = the padded counts of the groups with smaller expert ids,
+// each assignment's slot = start + its rank in its group -- and records the
+// groups in expert order; then every thread fills its share of the pads, the
+// tail and the block table.  Same output as the general path.
+MOE_DEV void align_few(const AlignArgs& a, int* sm) {
+  int* ge = sm;        // [32] expert of group g (expert order)
+  int* gs = sm + 32;   // [32] padded start
+  int* gc = sm + 64;   // [32] assignments
+  int* gt = sm + 96;   // [2] groups, padded total
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int E = a.E, BM = a.BM;
+  if (warp == 0) {
+    int e = -1;
+    if (lane < a.n) {
+      e = load_id(a.ids, lane, E);
+      if (e < 0) raise_error(a.err, kErrBadExpert);
+    }
+    const unsigned m = match_lanes(e, e >= 0, 32 - __clz(max(E - 1, 1)));
+    const bool leader = e >= 0 && lane == __ffs(m) - 1;
+    const int cnt = __popc(m);
+    const int pad = (cnt + BM - 1) / BM * BM;
+    int start = 0, g = 0;
+    for (int j = 0; j < 32; ++j) {
+      const int ej = __shfl_sync(0xffffffffu, e, j);
+      const int lj = __shfl_sync(0xffffffffu, leader ? 1 : 0, j);
+      const int pj = __shfl_sync(0xffffffffu, pad, j);
+      if (lj && ej < e) {
+        start += pj;
+        ++g;
+      }
+    }
+    if (e >= 0) {
+      const int pos = start + __popc(m & ((1u << lane) - 1u));
+      if (pos < a.cap) a.sorted[pos] = lane;
+    }
+    if (leader) {
+      ge[g] = e;
+      gs[g] = start;
+      gc[g] = cnt;
+    }
+    const int total = __reduce_add_sync(0xffffffffu, leader ? pad : 0);
+    const int ng = __popc(__ballot_sync(0xffffffffu, leader));
+    if (lane == 0) {
+      gt[0] = ng;
+      gt[1] = total;
+      *a.npp = total;
+    }
+  }
+  __syncthreads();
+  const int ng = gt[0], total = gt[1];
+  // pads inside the groups and the tail: n; data slots were written above
+  for (long long p = tid; p < a.cap; p += kAlignThreads) {
+    bool pad_slot = p >= total;
+    for (int g = 0; !pad_slot && g < ng; ++g)
+      if (p >= gs[g] + gc[g] && p < gs[g] + (gc[g] + BM - 1) / BM * BM) pad_slot = true;
+    if (pad_slot) a.sorted[p] = a.n;
+  }
+  for (long long b = tid; b < a.nbc; b += kAlignThreads) {
+    const long long p0 = b * BM;
+    int e = -1;
+    for (int g = 0; g < ng; ++g)
+      if (p0 >= gs[g] && p0 < gs[g] + (gc[g] + BM - 1) / BM * BM) e = ge[g];
+    a.blk[b] = e;
+  }
+}
+
 // Shared memory, 32-bit words: cnt[16][E] | tot[E] | start[E] | base[E] | wsum[32]
 inline size_t align_smem_bytes(int E) {
   return (static_cast<size_t>(kAlignWarps) * E + 3 * static_cast<size_t>(E) + 32) * 4;
@@ -83,6 +153,10 @@ inline size_t align_smem_bytes(int E) {
 
 __global__ void __launch_bounds__(kAlignThreads) align_kernel(const AlignArgs a) {
   extern __shared__ int sm[];
+  if (a.n <= 32) {
+    align_few(a, sm);
+    return;
+  }
   const int E = a.E, BM = a.BM;
   int* cnt = sm;                      // [16][E]: warp histogram, then running positions
   int* tot = cnt + kAlignWarps * E;   // [E] assignments per expert (whole problem)
@@ -249,7 +323,8 @@ int launch_align(const int32_t* topk_ids, int T, int k, int E, int block_m, int3
   a.G = (a.n + kAlignPerCta - 1) / kAlignPerCta;
   a.G = a.G < 1 ? 1 : (a.G > kAlignMaxCtas ? kAlignMaxCtas : a.G);
   a.seg = ((a.n + a.G - 1) / a.G + 31) / 32 * 32;
-  const size_t smem = align_smem_bytes(E);
+  // (align_few uses 98 words whatever E is)
+  const size_t smem = align_smem_bytes(E) > 512 ? align_smem_bytes(E) : 512;
   static bool attr_set = false;
   if (!attr_set) {
     if (cudaFuncSetAttribute(align_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -65,3 +65,13 @@ def test_bad_ids_are_flagged_not_written():
     real = sorted(int(a) for a in so if a < 6)
     assert real == [0, 1, 2, 5]
     assert moe.read_device_error(ws.buf) == 0  # cleared
+
+
+# At most 32 assignments (decode) take a one-warp path; 33 the general one.
+@pytest.mark.parametrize("T,k,E,BM", [(1, 1, 1, 16), (2, 1, 2, 16), (3, 1, 3, 64),
+                                      (4, 8, 16, 16), (4, 8, 128, 128), (31, 1, 5, 16),
+                                      (32, 1, 5, 64), (33, 1, 5, 16), (1, 8, 1024, 16),
+                                      (2, 8, 256, 128)])
+def test_few_assignments(T, k, E, BM):
+    ids, _ = W.random_routing(T, k, E, seed=T * 31 + E)
+    run_both(ids, E, BM)
