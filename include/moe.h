@@ -51,7 +51,11 @@ typedef enum {
   MOE_ERR_DEVICE = 4        /* returned by moe_read_device_error when set       */
 } moe_status;
 
-typedef enum { MOE_SCORING_SOFTMAX = 0, MOE_SCORING_SIGMOID = 1 } moe_scoring;
+typedef enum {
+  MOE_SCORING_SOFTMAX = 0,
+  MOE_SCORING_SIGMOID = 1,
+  MOE_SCORING_SQRT_SOFTPLUS = 2
+} moe_scoring;
 
 typedef enum { MOE_DT_BF16 = 0, MOE_DT_F32 = 1, MOE_DT_E4M3 = 2, MOE_DT_E2M1 = 3 } moe_dtype;
 
@@ -75,7 +79,11 @@ typedef enum { MOE_DT_BF16 = 0, MOE_DT_F32 = 1, MOE_DT_E4M3 = 2, MOE_DT_E2M1 = 3
  *                [T,H/32] (the router then sees the exact dequantised value)
  *   gate         [E,H] in gate_dt: BF16 or F32
  *   bias         [E] fp32 selection bias, or NULL for none
- *   scoring      MOE_SCORING_SOFTMAX (over all E logits) or _SIGMOID
+ *   scoring      MOE_SCORING_SOFTMAX (over all E logits), _SIGMOID, or
+ *                _SQRT_SOFTPLUS: sqrt(ln(1 + e^l)) per expert ([P1] §1.3:
+ *                DeepSeek-V4 takes the square root of a softplus in place
+ *                of the sigmoid; the rank key and weights follow as for the
+ *                sigmoid)
  *   n_group      1 = plain top-k; else E % n_group == 0, E/n_group >= 2,
  *                1 <= topk_group <= n_group, topk_group*E/n_group >= k
  *   renormalize  nonzero: w_j /= (sum_j w_j + 1e-20); then w_j *= scaling

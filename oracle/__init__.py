@@ -139,9 +139,12 @@ def decode(raw: np.ndarray, dtype: str, rows: int, cols: int, scale=None) -> np.
 
 # --- the method -------------------------------------------------------------
 
+SCORING = {"softmax": 0, "sigmoid": 1, "sqrt_softplus": 2}
+
+
 def router(x, x_dt, gate, gate_dt, bias, T, H, E, k, scoring, n_group=1, topk_group=1,
            renormalize=True, scaling=1.0, x_scale=None, tokens=None, want_logits=False):
-    """Routing of the listed tokens. scoring: 'softmax' | 'sigmoid'.
+    """Routing of the listed tokens. scoring: 'softmax' | 'sigmoid' | 'sqrt_softplus'.
 
     Returns (ids [n,k] int32, weights [n,k] f64, gap [n] f64[, logits [n,E]])."""
     lib = _load()
@@ -154,7 +157,7 @@ def router(x, x_dt, gate, gate_dt, bias, T, H, E, k, scoring, n_group=1, topk_gr
     gap = np.empty((n,), dtype=np.float64)
     logits = np.empty((n, E), dtype=np.float64) if want_logits else None
     rc = lib.orc_router(_ptr(x), DT[x_dt], _ptr(x_scale), _ptr(gate), DT[gate_dt], _ptr(b),
-                        T, H, E, k, {"softmax": 0, "sigmoid": 1}[scoring], n_group, topk_group,
+                        T, H, E, k, SCORING[scoring], n_group, topk_group,
                         int(bool(renormalize)), float(scaling), _ptr(tl), n, _ptr(ids), _ptr(w),
                         _ptr(logits), _ptr(gap))
     if rc != 0:

@@ -139,7 +139,8 @@ void orc_decode(const void* src, int dtype, const uint8_t* scale, int64_t row0,
 /* [P1] Section 1 "What the Router Computes" (three steps; rank key = score */
 /* + bias, weight = unbiased score, Figure 3), Section 4 (the five-line     */
 /* reference: sigmoid, top-k of score + bias, gather, divide by sum+1e-20), */
-/* Section 5.3 (k rounds, lowest id wins ties).                             */
+/* Section 5.3 (k rounds, lowest id wins ties); Section 1.3 (DeepSeek-V4    */
+/* scores with the square root of a softplus instead of a sigmoid).         */
 /* [P2] "Mixture of Experts", the gate and DeepSeek's grouped, bias-        */
 /* corrected routing (group score = sum of the two largest rank keys of the */
 /* group; keep topk_group groups; mask the rest to -inf; top-k; weights     */
@@ -152,7 +153,8 @@ static int beats(double ka, int ia, double kb, int ib) {
 }
 
 /* Router for the listed tokens (all tokens when token_list is NULL).
- *   scoring 0 = softmax over all E logits, 1 = sigmoid per expert.
+ *   scoring 0 = softmax over all E logits, 1 = sigmoid per expert,
+ *   2 = sqrt(softplus(l)) = sqrt(ln(1 + e^l)) per expert.
  *   n_group <= 1 means plain top-k.
  * Outputs, per listed token i (row i of the outputs):
  *   ids[i*k + j], weights[i*k + j] in selection order (best first);
@@ -164,7 +166,7 @@ int orc_router(const void* x, int x_dt, const uint8_t* x_scale, const void* gate
                const float* bias, int T, int H, int E, int k, int scoring, int n_group,
                int topk_group, int renormalize, double scaling, const int32_t* token_list,
                int n_tokens, int32_t* ids, double* weights, double* logits_out, double* gap) {
-  if (k < 1 || k > E || H < 1) return -1;
+  if (k < 1 || k > E || H < 1 || scoring < 0 || scoring > 2) return -1;
   if (n_group > 1 && (E % n_group != 0 || E / n_group < 2 || topk_group < 1 ||
                       topk_group > n_group || topk_group * (E / n_group) < k))
     return -1;
@@ -201,8 +203,14 @@ int orc_router(const void* x, int x_dt, const uint8_t* x_scale, const void* gate
         sum += s[e];
       }
       for (int e = 0; e < E; ++e) s[e] /= sum;
-    } else {
+    } else if (scoring == 1) {
       for (int e = 0; e < E; ++e) s[e] = 1.0 / (1.0 + exp(-l[e]));
+    } else {
+      /* softplus written so that neither exponential overflows */
+      for (int e = 0; e < E; ++e) {
+        const double sp = l[e] > 0.0 ? l[e] + log1p(exp(-l[e])) : log1p(exp(l[e]));
+        s[e] = sqrt(sp);
+      }
     }
     /* Rank key: score + selection bias (selection only). */
     for (int e = 0; e < E; ++e) {

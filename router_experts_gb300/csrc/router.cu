@@ -167,9 +167,14 @@ MOE_DEV void select_token(const RouterArgs& a, int t, const float* row, const fl
     const float inv = 1.0f / sum;
 #pragma unroll
     for (int i = 0; i < S; ++i) sc[i] *= inv;
-  } else {
+  } else if (a.scoring == 1) {
 #pragma unroll
     for (int i = 0; i < S; ++i) sc[i] = ok[i] ? 1.0f / (1.0f + expf(-sc[i])) : 0.f;
+  } else {
+    // sqrt(softplus(l)), softplus(l) = max(l, 0) + ln(1 + e^-|l|) (no overflow)
+#pragma unroll
+    for (int i = 0; i < S; ++i)
+      sc[i] = ok[i] ? sqrtf(fmaxf(sc[i], 0.f) + log1pf(expf(-fabsf(sc[i])))) : 0.f;
   }
 #pragma unroll
   for (int i = 0; i < S; ++i) {

@@ -61,7 +61,9 @@ extern "C" int moe_router_noalloc(const void* hidden, int hidden_dt, const uint8
   // the same argument rules as moe_router
   if (T < 0 || H <= 0 || E <= 0 || k <= 0) return MOE_ERR_ARG;
   if (k > E || k > 16 || E > 512 || H % 32 != 0) return MOE_ERR_ARG;
-  if (scoring != MOE_SCORING_SOFTMAX && scoring != MOE_SCORING_SIGMOID) return MOE_ERR_ARG;
+  if (scoring != MOE_SCORING_SOFTMAX && scoring != MOE_SCORING_SIGMOID &&
+      scoring != MOE_SCORING_SQRT_SOFTPLUS)
+    return MOE_ERR_ARG;
   if (n_group < 1 || n_group > 32) return MOE_ERR_ARG;
   if (n_group > 1 && (E % n_group != 0 || E / n_group < 2 || topk_group < 1 ||
                       topk_group > n_group || topk_group * (E / n_group) < k))

@@ -16,7 +16,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "_build", "libmoe.so")
 
 MOE_OK, MOE_ERR_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_DEVICE = 0, 1, 2, 3, 4
-SOFTMAX, SIGMOID = 0, 1
+SOFTMAX, SIGMOID, SQRT_SOFTPLUS = 0, 1, 2
+SCORING = {"softmax": SOFTMAX, "sigmoid": SIGMOID, "sqrt_softplus": SQRT_SOFTPLUS}
 DT_BF16, DT_F32, DT_E4M3, DT_E2M1 = 0, 1, 2, 3
 DEVERR_BAD_EXPERT_ID, DEVERR_WAIT_TIMEOUT, DEVERR_BAD_TABLE = 1, 2, 4
 
@@ -168,7 +169,7 @@ def router(hidden, gate, bias, k, scoring="softmax", n_group=1, topk_group=1, re
     buf = ws.get(lib.moe_router_workspace_bytes(T, H, E))
     rc = lib.moe_router(_p(hidden), _dt(hidden, hidden_scale), _p(hidden_scale), _p(gate),
                         _dt(gate, None), _p(bias), T, H, E, k,
-                        SOFTMAX if scoring == "softmax" else SIGMOID, n_group, topk_group,
+                        SCORING[scoring], n_group, topk_group,
                         int(bool(renormalize)), float(scaling), _p(ids), _p(wts), _p(buf),
                         buf.numel(), _stream(dev))
     _check(rc, "moe_router")
@@ -293,7 +294,7 @@ def layer(hidden, gate, bias, w13, w2, k, scoring="softmax", n_group=1, topk_gro
     buf = ws.get(lib.moe_layer_workspace_bytes(T, H, F, E, k, block_m, act_dt))
     rc = lib.moe_layer(_p(hidden), act_dt, _p(hidden_scale), _p(gate), _dt(gate, None), _p(bias),
                        _p(w13), _p(w13_scale), _p(w2), _p(w2_scale), _wdt(w13), T, H, F, E, k,
-                       SOFTMAX if scoring == "softmax" else SIGMOID, n_group, topk_group,
+                       SCORING[scoring], n_group, topk_group,
                        int(bool(renormalize)), float(scaling), block_m, _p(out), _p(buf),
                        buf.numel(), _stream(dev))
     _check(rc, "moe_layer")

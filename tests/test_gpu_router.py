@@ -2,6 +2,8 @@
 inputs: ids identical (in selection order) for every token whose margin at
 the cut exceeds 1e-4, weights within 1e-5 absolute; the residual mismatch
 fraction is reported."""
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -19,9 +21,7 @@ CASES = [("toy", 16), ("toy", 5), ("qwen3", 1), ("qwen3", 64), ("qwen3", 512), (
          ("glm", 512), ("glm", 4096), ("v4lo", 512), ("v4lo", 4096)]
 
 
-@pytest.mark.parametrize("name,T", CASES)
-def test_router_matches_oracle(name, T):
-    w = W.WORKLOADS[name]
+def check_router(w, T):
     d = W.make_inputs(w, T, seed=T, device="cuda", experts=False)
     ids, wts = moe.router(d["hidden"], d["gate"], d.get("bias"), w.k, w.scoring, w.n_group,
                           w.topk_group, w.renormalize, w.scaling,
@@ -34,11 +34,25 @@ def test_router_matches_oracle(name, T):
     clear = gap > GAP_MIN
     same = (ids_g == ids_o).all(axis=1)
     mismatch = 1.0 - same.mean()
-    print(f"{name} T={T}: {len(tokens)} tokens, {clear.mean():.3f} clear of the 1e-4 cut, "
+    print(f"{w.name} {w.scoring} T={T}: {len(tokens)} tokens, {clear.mean():.3f} clear of the 1e-4 cut, "
           f"mismatch fraction {mismatch:.4f}")
     assert same[clear].all(), np.nonzero(clear & ~same)
     assert np.abs(w_g[same] - w_o[same]).max() <= WEIGHT_ATOL
     assert clear.mean() > 0.5  # the comparison is not vacuous
+
+
+@pytest.mark.parametrize("name,T", CASES)
+def test_router_matches_oracle(name, T):
+    check_router(W.WORKLOADS[name], T)
+
+
+# DeepSeek-V4's score, the square root of a softplus, through both router
+# paths (tensor-core pair; one launch for the fp32 gate below 8 tokens) and
+# the grouped selection.
+@pytest.mark.parametrize("name,T", [("qwen3", 1), ("qwen3", 64), ("qwen3", 4096), ("dsv3", 1),
+                                    ("dsv3", 256), ("glm", 8), ("v4lo", 1), ("v4lo", 512)])
+def test_router_sqrt_softplus(name, T):
+    check_router(dataclasses.replace(W.WORKLOADS[name], scoring="sqrt_softplus"), T)
 
 
 def test_router_ties_lowest_id_and_renorm():

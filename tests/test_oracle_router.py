@@ -8,6 +8,9 @@
   over the selected logits only ("Mixture of Experts", fused_topk discussion).
 * Brute force: group-limited top-k by exhaustive enumeration on tiny E.
 * Ties: lowest expert id wins ("MoE Kernels, in depth", Router section).
+* The square root of a softplus (§1.3, DeepSeek-V4's score): sqrt(ln 2) at a
+  zero logit, the sqrt(l) and e^(l/2) asymptotes, and the same ranking as the
+  sigmoid when there is no bias (both increase with the logit).
 """
 import itertools
 import json
@@ -191,3 +194,23 @@ def test_gap_definition():
     gsc = [s[0] + s[1], s[2] + s[3], s[4] + s[5], s[6] + s[7]]
     assert list(ids[0]) == [4, 5]
     assert gap[0] == pytest.approx(gsc[2] - gsc[0], abs=1e-15)
+
+
+def test_sqrt_softplus_scores_at_known_points():
+    # unnormalised weights are the scores: sqrt(ln(1 + e^l))
+    ids, w, gap, _ = route_logits([[0.0, 30.0, -30.0, 2.0]], None, 4, scoring="sqrt_softplus",
+                                  renorm=False)
+    s = dict(zip(ids[0].tolist(), w[0].tolist()))
+    assert abs(s[0] - 0.8325546111576977) < 1e-12          # sqrt(ln 2)
+    assert abs(s[1] - math.sqrt(30.0)) < 1e-10             # softplus(l) - l = ln(1 + e^-l)
+    assert abs(s[2] / math.exp(-15.0) - 1.0) < 1e-6        # softplus(l) ~ e^l for l << 0
+    assert list(ids[0]) == [1, 3, 0, 2]                    # increasing in the logit
+
+
+def test_sqrt_softplus_ranks_like_sigmoid_without_bias():
+    rng = np.random.default_rng(5)
+    logits = rng.normal(size=(64, 24)).astype(np.float32)
+    a = route_logits(logits, None, 6, scoring="sigmoid")
+    b = route_logits(logits, None, 6, scoring="sqrt_softplus")
+    assert np.array_equal(a[0], b[0])
+    assert np.allclose(b[1].sum(axis=1), 1.0)
