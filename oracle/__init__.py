@@ -83,6 +83,8 @@ def _load():
             lib.orc_moe_ffn.restype = i32
             lib.orc_moe_ffn.argtypes = [P, i32, P, P, P, P, P, i32, i32, i32, i32, i32, i32,
                                         P, P, P, i32, i32, P]
+            lib.orc_quantize_e4m3.restype = i32
+            lib.orc_quantize_e4m3.argtypes = [P, i32, i32, i32, P, P]
             lib.orc_num_threads.restype = i32
             lib.orc_num_threads.argtypes = []
             _lib = lib
@@ -163,6 +165,17 @@ def router(x, x_dt, gate, gate_dt, bias, T, H, E, k, scoring, n_group=1, topk_gr
     if rc != 0:
         raise ValueError("oracle router: invalid arguments")
     return (ids, w, gap, logits) if want_logits else (ids, w, gap)
+
+
+def quantize_e4m3(x, x_dt, T, H):
+    """FP8 cast of a [T, H] bf16 or f32 array: (codes [T, H] uint8, scale bytes
+    [T, H/32] uint8), per 32 values the smallest 2^s with amax / 2^s <= 448."""
+    x = _raw(x)
+    codes = np.empty((T, H), dtype=np.uint8)
+    scales = np.empty((T, H // 32), dtype=np.uint8)
+    if _load().orc_quantize_e4m3(_ptr(x), DT[x_dt], T, H, _ptr(codes), _ptr(scales)) != 0:
+        raise ValueError("oracle quantize_e4m3: invalid arguments")
+    return codes, scales
 
 
 def align(topk_ids, T, k, E, block_m, cap_rows=None):

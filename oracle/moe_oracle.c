@@ -432,6 +432,58 @@ int orc_moe_ffn(const void* x, int x_dt, const uint8_t* x_scale, const void* w13
 }
 
 /* Number of threads OpenMP would use (for reporting). */
+/* ------------------------------------------------------------------------ */
+/* FP8 cast of the layer input.                                             */
+/* "How GPUs Fuse Communication and Computation During LLM Inference" §1.1  */
+/* (a small cast kernel turns the layer input into FP8 codes and writes the */
+/* scales) with the scale rule of §3.5 (per 32 values, the smallest power   */
+/* of two 2^s with amax / 2^s <= 448; codes = e4m3(value / 2^s), nearest,   */
+/* ties to even, saturating); "MoE Kernels, in depth", Low precision (the   */
+/* activation quantisation belongs in a pass that moves the rows anyway).   */
+/* ------------------------------------------------------------------------ */
+
+/* e4m3 code of a value that is already an e4m3 value (or +-0): the code in
+ * the 256-entry table whose value it is (sign from the sign bit, so -0 is
+ * 0x80).  Returns 0xFF (a NaN code) if there is none. */
+static uint8_t e4m3_code_of(double q) {
+  const int neg = signbit(q) ? 1 : 0;
+  const double a = fabs(q);
+  for (int c = 0; c < 128; ++c)
+    if (c != 0x7F && orc_e4m3_to_double((uint8_t)c) == a) return (uint8_t)(c | (neg << 7));
+  return 0xFF;
+}
+
+/* codes [T*H] and scale bytes [T*H/32] of x [T,H] (bf16 or f32), H % 32 == 0.
+ * s is found by stepping from -127 (the smallest UE8M0 exponent) upward, so it
+ * is the smallest s in [-127, 127] with amax <= 448 * 2^s (s = 0 for an
+ * all-zero group).  Returns 0, or -1 on invalid arguments. */
+int orc_quantize_e4m3(const void* x, int x_dt, int T, int H, uint8_t* codes, uint8_t* scales) {
+  if (T < 0 || H <= 0 || H % 32 != 0 || (x_dt != 0 && x_dt != 1)) return -1;
+  int bad = 0;
+#pragma omp parallel for schedule(static)
+  for (int t = 0; t < T; ++t) {
+    for (int g = 0; g < H / 32; ++g) {
+      double v[32], amax = 0.0;
+      for (int i = 0; i < 32; ++i) {
+        v[i] = elem(x, x_dt, NULL, t, H, g * 32 + i);
+        if (fabs(v[i]) > amax) amax = fabs(v[i]);
+      }
+      int s = 0;
+      if (amax > 0.0) {
+        s = -127;
+        while (s < 127 && amax > 448.0 * ldexp(1.0, s)) ++s;
+      }
+      scales[(int64_t)t * (H / 32) + g] = (uint8_t)(s + 127);
+      for (int i = 0; i < 32; ++i) {
+        const uint8_t c = e4m3_code_of(orc_round_e4m3(v[i] / ldexp(1.0, s)));
+        if (c == 0xFF) bad = 1;
+        codes[(int64_t)t * H + g * 32 + i] = c;
+      }
+    }
+  }
+  return bad ? -1 : 0;
+}
+
 int orc_num_threads(void) {
 #ifdef _OPENMP
   extern int omp_get_max_threads(void);
