@@ -592,7 +592,8 @@ def run_ours(args):
         "sweep": sweep,
         "e2e": e2e,
         "gpu_launches": K * moe.layer_kernel_count(
-            T, H, F, E, k, "e4m3" if w.lowbit else "bf16", "f32" if w.lowbit else "bf16"),
+            T, H, F, E, k, "e4m3" if w.lowbit else "bf16", "f32" if w.lowbit else "bf16",
+            "e2m1" if w.lowbit else "bf16"),
         "cpu_baseline": cpu,
         "device_error_word": code,
     }

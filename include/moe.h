@@ -239,17 +239,35 @@ int moe_grouped_ffn(const void* x, const uint8_t* x_scale, int act_dt, const voi
 int moe_finalize(const void* stage, int T, int k, int H, void* out, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * FP8 cast of a layer input.  [P4] §1.1 (a small kernel converts the layer
+ * input to FP8 and writes the scales) with §3.5's scale rule; [P3] "Low
+ * precision" (quantise activations in a pass that moves the rows anyway).
+ *   x      [T,H] bf16, 16-byte aligned, H % 32 == 0
+ *   codes  [T,H] e4m3 out, 16-byte aligned
+ *   scales [T,H/32] UE8M0 out: per 32 values the smallest 2^s (s in
+ *          [-127, 127], 0 for an all-zero group) with amax / 2^s <= 448
+ *   codes = e4m3(x / 2^s), nearest, ties to even, saturating at 448.
+ * MOE_ERR_ARG for invalid shapes or alignment; T == 0 is a no-op.
+ * ------------------------------------------------------------------------- */
+int moe_cast_e4m3(const void* x, int T, int H, uint8_t* codes, uint8_t* scales, void* stream);
+
+/* ---------------------------------------------------------------------------
  * The whole layer: router, align, GEMM1 + SwiGLU, GEMM2 + weight, finalize,
  * enqueued back to back with no host synchronisation.  block_m = 0 picks the
  * tile height from the mean rows per expert T*k/E: 16 below 8, 64 below 64,
  * else 128 ([P3] "Tile shape is the main tuning knob ... depends on tokens
  * per expert").  act_dt/w_dt as for the expert GEMMs; the router reads
  * `hidden` (dequantised when E4M3).  out [T,H] bf16.
+ * act_dt BF16 with w_dt E2M1 (hidden_scale ignored): the router reads the
+ * bf16 rows and the experts read their FP8 cast (moe_cast_e4m3, enqueued
+ * between align and GEMM1; [P4] §1.1 puts that cast in front of the fused
+ * expert kernel); hidden must be 16-byte aligned.
  * moe_layer_kernel_count returns how many kernels moe_layer enqueues for
  * these shapes and types (0 when T == 0 or the arguments are invalid).
  * ------------------------------------------------------------------------- */
 size_t moe_layer_workspace_bytes(int T, int H, int F, int E, int k, int block_m, int act_dt);
-int moe_layer_kernel_count(int T, int H, int F, int E, int k, int act_dt, int gate_dt);
+int moe_layer_kernel_count(int T, int H, int F, int E, int k, int act_dt, int gate_dt,
+                           int w_dt);
 int moe_layer(const void* hidden, int act_dt, const uint8_t* hidden_scale, const void* gate,
               int gate_dt, const float* bias, const void* w13, const uint8_t* w13_scale,
               const void* w2, const uint8_t* w2_scale, int w_dt, int T, int H, int F, int E,

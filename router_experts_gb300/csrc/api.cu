@@ -61,7 +61,7 @@ static FfnLayout ffn_layout(int T, int F, int E, int k, int block_m, bool with_i
 }
 
 struct LayerLayout {
-  size_t ids, wts, sorted, blk, npp, stage, router, ffn, total;
+  size_t ids, wts, sorted, blk, npp, stage, router, ffn, xq, xs, total;
   int64_t cap;
 };
 static LayerLayout layer_layout(int T, int H, int F, int E, int k, int block_m,
@@ -86,6 +86,15 @@ static LayerLayout layer_layout(int T, int H, int F, int E, int k, int block_m,
   off += plan_router(T, H, E).scratch_bytes;
   L.ffn = off;
   off += ffn_layout(T, F, E, k, block_m, true, act_dt).total;
+  // a bf16 hidden may feed low-bit experts: room for its FP8 cast (the
+  // low-bit intermediate is smaller than the bf16 one reserved above)
+  L.xq = L.xs = 0;
+  if (act_dt == MOE_DT_BF16) {
+    L.xq = off;
+    off += align_up(static_cast<size_t>(T) * H, 256);
+    L.xs = off;
+    off += align_up(static_cast<size_t>(T) * (H / 32), 256);
+  }
   L.total = off;
   return L;
 }
@@ -440,6 +449,16 @@ int moe_finalize(const void* stage, int T, int k, int H, void* out, void* stream
   return MOE_OK;
 }
 
+// ---- FP8 cast -------------------------------------------------------------------
+int moe_cast_e4m3(const void* x, int T, int H, uint8_t* codes, uint8_t* scales, void* stream) {
+  if (T < 0 || H <= 0 || H % 32 != 0) return MOE_ERR_ARG;
+  if (T == 0) return MOE_OK;
+  if (!x || !codes || !scales || !aligned(x, 16) || !aligned(codes, 16)) return MOE_ERR_ARG;
+  if (launch_cast_e4m3(x, T, H, codes, scales, static_cast<cudaStream_t>(stream)) != 0)
+    return launch_fail("cast kernel");
+  return MOE_OK;
+}
+
 // ---- layer ------------------------------------------------------------------------
 size_t moe_layer_workspace_bytes(int T, int H, int F, int E, int k, int block_m, int act_dt) {
   if (T < 0 || H <= 0 || F <= 0 || E <= 0 || k <= 0) return 0;
@@ -448,10 +467,13 @@ size_t moe_layer_workspace_bytes(int T, int H, int F, int E, int k, int block_m,
   return layer_layout(T, H, F, E, k, block_m, act_dt).total;
 }
 
-int moe_layer_kernel_count(int T, int H, int F, int E, int k, int act_dt, int gate_dt) {
+int moe_layer_kernel_count(int T, int H, int F, int E, int k, int act_dt, int gate_dt,
+                           int w_dt) {
   if (T <= 0 || H <= 0 || F <= 0 || E <= 0 || k <= 0) return 0;
-  // router + align, GEMM1, GEMM2, finalize
-  return moe_router_kernel_count(T, H, E, act_dt, gate_dt) + 4;
+  // router + align, GEMM1, GEMM2, finalize (+ the FP8 cast of a bf16 hidden
+  // for e2m1 experts)
+  const int cast = (act_dt == MOE_DT_BF16 && w_dt == MOE_DT_E2M1) ? 1 : 0;
+  return moe_router_kernel_count(T, H, E, act_dt, gate_dt) + 4 + cast;
 }
 
 int moe_layer(const void* hidden, int act_dt, const uint8_t* hidden_scale, const void* gate,
@@ -464,10 +486,15 @@ int moe_layer(const void* hidden, int act_dt, const uint8_t* hidden_scale, const
                         n_group, topk_group);
   if (rc != MOE_OK) return rc;
   const LayerLayout L = layer_layout(T, H, F, E, k, block_m, act_dt);
-  rc = check_ffn(act_dt, w_dt, T, H, F, E, k, block_m, L.cap);
+  // a bf16 hidden with e2m1 experts: the router reads the bf16 rows, the
+  // experts their FP8 cast (made here, in front of the expert GEMMs)
+  const bool cast_input = act_dt == MOE_DT_BF16 && w_dt == MOE_DT_E2M1;
+  const int ffn_dt = cast_input ? MOE_DT_E4M3 : act_dt;
+  rc = check_ffn(ffn_dt, w_dt, T, H, F, E, k, block_m, L.cap);
   if (rc != MOE_OK) return rc;
   if (T == 0) return MOE_OK;
   if (!out || !ws || !w13 || !w2) return MOE_ERR_ARG;
+  if (cast_input && !aligned(hidden, 16)) return MOE_ERR_ARG;
   if (ws_bytes < L.total || !aligned(ws, 256)) return MOE_ERR_ARG;
   char* base = static_cast<char*>(ws);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -487,13 +514,22 @@ int moe_layer(const void* hidden, int act_dt, const uint8_t* hidden_scale, const
   if (launch_align(ids, T, k, E, block_m, sorted, L.cap, blk, npp, align_hist(ws), align_bar(ws),
                    err_word(ws), s) != 0)
     return launch_fail("align kernel");
-  const FfnLayout FL = ffn_layout(T, F, E, k, block_m, true, act_dt);
+  const FfnLayout FL = ffn_layout(T, F, E, k, block_m, true, ffn_dt);
   void* inter = base + L.ffn + FL.inter;
-  if (act_dt == MOE_DT_E4M3) {
-    if (!hidden_scale || !w13_scale || !w2_scale) return MOE_ERR_ARG;
+  if (ffn_dt == MOE_DT_E4M3) {
+    const void* xq = hidden;
+    const uint8_t* xs = hidden_scale;
+    if (cast_input) {
+      uint8_t* cq = reinterpret_cast<uint8_t*>(base + L.xq);
+      uint8_t* cs = reinterpret_cast<uint8_t*>(base + L.xs);
+      if (launch_cast_e4m3(hidden, T, H, cq, cs, s) != 0) return launch_fail("cast kernel");
+      xq = cq;
+      xs = cs;
+    }
+    if (!xs || !w13_scale || !w2_scale) return MOE_ERR_ARG;
     uint8_t* iq = static_cast<uint8_t*>(inter);
     uint8_t* isc = iq + align_up(static_cast<size_t>(L.cap) * F, 256);
-    rc = expert_gemm_lowbit(0, hidden, hidden_scale, w13, w13_scale, T, H, F, E, k, block_m,
+    rc = expert_gemm_lowbit(0, xq, xs, w13, w13_scale, T, H, F, E, k, block_m,
                             sorted, blk, npp, L.cap, iq, isc, nullptr, nullptr, ws, s);
     if (rc != MOE_OK) return rc;
     rc = expert_gemm_lowbit(1, iq, isc, w2, w2_scale, T, H, F, E, k, block_m, sorted, blk, npp,

@@ -98,6 +98,10 @@ struct LowbitParams {
   int cap_rows;
 };
 int launch_lowbit_gemm(int kind, const LowbitParams& p, int num_sms, cudaStream_t stream);
+// bf16 x [T, H] (16-byte aligned, H % 32 == 0) -> e4m3 codes [T, H] (16-byte
+// aligned) and UE8M0 scale bytes [T, H/32].
+int launch_cast_e4m3(const void* x, int T, int H, uint8_t* codes, uint8_t* scales,
+                     cudaStream_t stream);
 
 // ---- finalize -----------------------------------------------------------------
 int launch_finalize(const void* stage, int T, int k, int H, void* out, cudaStream_t stream);

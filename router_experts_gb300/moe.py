@@ -49,7 +49,8 @@ def load():
         sig = {
             "moe_router_workspace_bytes": (SZ, [I, I, I]),
             "moe_router_kernel_count": (I, [I, I, I, I, I]),
-            "moe_layer_kernel_count": (I, [I, I, I, I, I, I, I]),
+            "moe_layer_kernel_count": (I, [I, I, I, I, I, I, I, I]),
+            "moe_cast_e4m3": (I, [P, I, I, P, P, P]),
             "moe_router": (I, [P, I, P, P, I, P, I, I, I, I, I, I, I, I, F, P, P, P, SZ, P]),
             "moe_align_workspace_bytes": (SZ, []),
             "moe_align": (I, [P, I, I, I, I, P, I64, P, P, P, SZ, P]),
@@ -147,10 +148,22 @@ def router_kernel_count(T: int, H: int, E: int, hidden_dtype="bf16", gate_dtype=
 
 
 def layer_kernel_count(T: int, H: int, F: int, E: int, k: int, act_dtype="bf16",
-                       gate_dtype="bf16") -> int:
+                       gate_dtype="bf16", weight_dtype="bf16") -> int:
     """Kernels moe_layer enqueues for these shapes and types."""
-    dt = {"bf16": DT_BF16, "f32": DT_F32, "e4m3": DT_E4M3}
-    return int(load().moe_layer_kernel_count(T, H, F, E, k, dt[act_dtype], dt[gate_dtype]))
+    dt = {"bf16": DT_BF16, "f32": DT_F32, "e4m3": DT_E4M3, "e2m1": DT_E2M1}
+    return int(load().moe_layer_kernel_count(T, H, F, E, k, dt[act_dtype], dt[gate_dtype],
+                                             dt[weight_dtype]))
+
+
+def cast_e4m3(x):
+    """bf16 [T, H] -> (e4m3 codes [T, H] uint8, UE8M0 scale bytes [T, H/32] uint8)."""
+    lib = load()
+    T, H = x.shape
+    codes = torch.empty((T, H), dtype=torch.uint8, device=x.device)
+    scales = torch.empty((T, H // 32), dtype=torch.uint8, device=x.device)
+    _check(lib.moe_cast_e4m3(_p(x), T, H, _p(codes), _p(scales), _stream(x.device)),
+           "moe_cast_e4m3")
+    return codes, scales
 
 
 # ---- entry points ---------------------------------------------------------------

@@ -142,3 +142,58 @@ def test_lowbit_small_shapes(T, E, k, H, F, BM, off):
     err = rel_err(y.float().cpu().numpy(), ref)
     print(f"low-bit T={T} E={E} k={k} H={H} F={F} BM={BM} scale offset {off}: rel err {err:.2e}")
     assert err <= LAYER_RTOL_LOWBIT
+
+
+# ---- FP8 cast of a bf16 layer input ("How GPUs Fuse ..." §1.1, §3.5) ---------
+
+def test_cast_is_bit_exact_against_the_oracle():
+    T, H = 300, 512
+    g = torch.Generator(device="cpu").manual_seed(9)
+    x = torch.randn((T, H), generator=g, dtype=torch.float32)
+    # per-group magnitudes from 2^-140 (bf16 subnormals: the scale clamps at
+    # 2^-127) to 2^60, an all-zero group, negative zeros, exact 448 multiples
+    mag = torch.exp2(torch.randint(-140, 61, (T, H // 32), generator=g).float())
+    x = x * mag.repeat_interleave(32, dim=1)
+    x[0, :32] = 0.0
+    x[1, :32] = -0.0
+    x[2, :32] = 448.0 * 2.0 ** 5
+    x[3, 5] = -0.0
+    xb = x.to(torch.bfloat16)
+    codes, scales = moe.cast_e4m3(xb.cuda())
+    torch.cuda.synchronize()
+    co, so = oracle.quantize_e4m3(host(xb), "bf16", T, H)
+    assert np.array_equal(scales.cpu().numpy(), so)
+    assert np.array_equal(codes.cpu().numpy(), co)
+    assert scales[2, 0].item() == 127 + 5 and scales[0, 0].item() == 127
+
+
+@pytest.mark.parametrize("T,ntok", [(1, 1), (64, 16), (512, 12)])
+def test_bf16_input_lowbit_layer_matches_oracle(T, ntok):
+    w = W.WORKLOADS["v4lo"]
+    d = v4lo_inputs(T, seed=4)
+    g = torch.Generator(device="cuda").manual_seed(T)
+    xb = torch.randn((T, w.H), generator=g, device="cuda", dtype=torch.float32).to(torch.bfloat16)
+    y = moe.layer(xb, d["gate"], d["bias"], d["w13"], d["w2"], w.k, w.scoring,
+                  renormalize=w.renormalize, scaling=w.scaling, w13_scale=d["w13_scale"],
+                  w2_scale=d["w2_scale"])
+    torch.cuda.synchronize()
+    assert moe.layer_kernel_count(T, w.H, w.F, w.E, w.k, "bf16", "f32", "e2m1") == \
+        moe.router_kernel_count(T, w.H, w.E, "bf16", "f32") + 5
+    tokens = sample_tokens(T, ntok, seed=T)
+    # the router reads the bf16 rows; the experts read the oracle's own cast
+    ids_o, w_o, gap = oracle.router(host(xb), "bf16", host(d["gate"]), "f32",
+                                    d["bias"].cpu().numpy(), T, w.H, w.E, w.k, w.scoring,
+                                    renormalize=w.renormalize, scaling=w.scaling, tokens=tokens)
+    keep = gap > GAP_MIN
+    tokens, ids_o, w_o = tokens[keep], ids_o[keep], w_o[keep]
+    codes, scales = oracle.quantize_e4m3(host(xb), "bf16", T, w.H)
+    w13h, w2h, rid, En, s13, s2 = compact_experts(d["w13"], d["w2"], ids_o, d["w13_scale"],
+                                                  d["w2_scale"])
+    ref = oracle.moe_ffn(codes[tokens], "e4m3", w13h, w2h, "e2m1", len(tokens), w.H, w.F, En,
+                         w.k, rid, np.asarray(w_o, np.float64), x_scale=scales[tokens],
+                         w13_scale=s13, w2_scale=s2)
+    got = y.float().cpu().numpy()[tokens]
+    err = rel_err(got, ref)
+    print(f"bf16-input low-bit layer T={T}: {len(tokens)} tokens, rel err {err:.2e}")
+    assert len(tokens) > 0 and np.isfinite(got).all()
+    assert err <= LAYER_RTOL_LOWBIT
