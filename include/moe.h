@@ -262,6 +262,10 @@ int moe_cast_e4m3(const void* x, int T, int H, uint8_t* codes, uint8_t* scales, 
  * bf16 rows and the experts read their FP8 cast (moe_cast_e4m3, enqueued
  * between align and GEMM1; [P4] §1.1 puts that cast in front of the fused
  * expert kernel); hidden must be 16-byte aligned.
+ * One token (T == 1) skips the align launch: its k experts are distinct, so
+ * every block holds one assignment and the GEMMs read topk_ids as the block
+ * table ([P2] "vLLM's Triton path": the naive block assignment of small
+ * batches).
  * moe_layer_kernel_count returns how many kernels moe_layer enqueues for
  * these shapes and types (0 when T == 0 or the arguments are invalid).
  * ------------------------------------------------------------------------- */

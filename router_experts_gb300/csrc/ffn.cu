@@ -106,9 +106,7 @@ template <int KIND, int BM>
 MOE_DEV Sched make_sched(const FfnParams& p) {
   using C = Cfg<KIND, BM>;
   Sched s;
-  int npp = __ldg(p.num_post_padded);
-  npp = max(0, min(npp, p.cap_rows));
-  s.nblk = npp / BM;
+  s.nblk = padded_rows(p, BM) / BM;
   s.ntiles = (KIND == 0) ? (p.F + C::NT - 1) / C::NT : (p.H + C::NT - 1) / C::NT;
   const int K = (KIND == 0) ? p.H : p.F;
   s.KB = (K + kBK - 1) / kBK;
@@ -206,7 +204,7 @@ MOE_DEV void epilogue_tile(const FfnParams& p, const Unit& u, int row, Fetch&& f
       fetch(c0, v);
 #pragma unroll
       for (int c = 0; c < 16; ++c) {
-        const int a = __ldg(p.sorted_ids + static_cast<size_t>(u.b) * BM + c0 + c);
+        const int a = row_assignment(p, u.b, BM, c0 + c);
         if (a >= 0 && a < nk && h < p.H) {
           const float w = __ldg(p.topk_weights + a);
           stage[static_cast<size_t>(a) * p.H + h] = __float2bfloat16_rn(v[c] * w);
@@ -227,7 +225,7 @@ MOE_DEV void epilogue_rows128(const FfnParams& p, const Unit& u, int row, uint32
   bool valid = true;
   float w = 1.f;
   if constexpr (KIND == 1) {
-    a = __ldg(p.sorted_ids + prow);
+    a = row_assignment(p, u.b, 128, row);
     valid = a >= 0 && a < p.T * p.k;
     w = valid ? __ldg(p.topk_weights + a) : 0.f;
   }
@@ -424,7 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < C::G_PER_THREAD; ++i) {
           const int r = (gt >> 3) + 8 * i;
-          const int a = __ldg(p.sorted_ids + static_cast<size_t>(u.b) * BM + r);
+          const int a = row_assignment(p, u.b, BM, r);
           const bool valid = a >= 0 && a < nk;
           src[i] = valid ? x + static_cast<size_t>(a / p.k) * p.H + chunk * 8 : x;
           nbytes[i] = valid ? 16u : 0u;

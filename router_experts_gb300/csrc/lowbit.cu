@@ -170,9 +170,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int K = (KIND == 0) ? p.H : p.F;
   const int KS = K / kMxBK;
-  int npp = __ldg(p.num_post_padded);
-  npp = max(0, min(npp, p.cap_rows));
-  const int nblk = npp / p.BM;
+  const int nblk = padded_rows(p, p.BM) / p.BM;
   const int ntiles = (KIND == 0) ? p.F / (kMxNT / 2) : p.H / kMxNT;
   const int num_units = nblk * ntiles;
   const int bmr = min(p.BM, 128);  // token rows of a tile that hold data
@@ -212,7 +210,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   // token row of tile row r (GEMM1), or -1 for a padding row
   auto token_of = [&](const MxUnit& u, int r) -> int {
     if (r >= p.BM) return -1;
-    const int a = __ldg(p.sorted_ids + static_cast<size_t>(u.b) * p.BM + r);
+    const int a = row_assignment(p, u.b, p.BM, r);
     return (a >= 0 && a < p.T * p.k) ? a / p.k : -1;
   };
 
@@ -479,7 +477,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
         }
       } else {
         int a = p.T * p.k;
-        if (rvalid) a = __ldg(p.sorted_ids + prow);
+        if (rvalid) a = row_assignment(p, u.b, p.BM, row);
         const bool valid = rvalid && a >= 0 && a < p.T * p.k;
         const float w = valid ? __ldg(p.topk_weights + a) : 0.f;
 #pragma unroll 1

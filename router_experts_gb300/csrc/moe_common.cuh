@@ -101,6 +101,24 @@ MOE_DEV void tma_prefetch_l2_2d(const CUtensorMap* map, int c0, int c1) {
 }
 
 // ---------------------------------------------------------------------------
+// Block tables of the expert GEMMs.  Normally the align outputs: padded
+// length, block_expert, sorted_ids.  With `naive` set (one token: "Mixture
+// of Experts", vLLM's path that skips the alignment), every block holds one
+// assignment: block b is assignment b in row 0 (padding in the other rows),
+// block_expert is topk_ids itself, and the padded length is T*k*BLOCK_M.
+// ---------------------------------------------------------------------------
+template <class P>
+MOE_DEV int padded_rows(const P& p, int bm) {
+  const int npp = p.naive ? p.T * p.k * bm : __ldg(p.num_post_padded);
+  return max(0, min(npp, p.cap_rows));
+}
+template <class P>
+MOE_DEV int row_assignment(const P& p, int b, int bm, int r) {
+  if (p.naive) return r == 0 ? b : p.T * p.k;
+  return __ldg(p.sorted_ids + static_cast<size_t>(b) * bm + r);
+}
+
+// ---------------------------------------------------------------------------
 // cp.async (16-byte global -> shared, zero-filled when src_bytes == 0)
 // ---------------------------------------------------------------------------
 MOE_DEV void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes) {

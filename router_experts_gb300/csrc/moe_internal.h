@@ -73,6 +73,7 @@ struct FfnParams {
   int T, H, F, E, k;
   int cap_rows;
   int max_slots;               // capacity of `partial`, in units
+  int naive;                   // single-assignment blocks (see padded_rows)
 };
 int ffn_max_slots(int block_m);
 size_t ffn_partial_bytes(int block_m);
@@ -96,6 +97,7 @@ struct LowbitParams {
   int* err;
   int T, H, F, E, k, BM;
   int cap_rows;
+  int naive;                   // single-assignment blocks (see padded_rows)
 };
 int launch_lowbit_gemm(int kind, const LowbitParams& p, int num_sms, cudaStream_t stream);
 // bf16 x [T, H] (16-byte aligned, H % 32 == 0) -> e4m3 codes [T, H] (16-byte

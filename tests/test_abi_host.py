@@ -117,14 +117,16 @@ def test_align_and_ffn_reject_bad_arguments(lib):
 def test_layer_kernel_count(lib):
     # router launches (two for bf16 hidden and gate; one below 8 tokens for an
     # fp32 gate; conversion + GEMM + selection for e4m3 hidden with an fp32
-    # gate; one for more experts than the tensor-core router covers), then
-    # align, GEMM1, GEMM2 and finalize
-    assert lib.moe_layer_kernel_count(1, 2048, 768, 128, 8, 0, 0, 0) == 6
+    # gate; one for more experts than the tensor-core router covers), align
+    # except for one token (single-assignment blocks), GEMM1, GEMM2, finalize
+    assert lib.moe_layer_kernel_count(1, 2048, 768, 128, 8, 0, 0, 0) == 5
+    assert lib.moe_layer_kernel_count(2, 2048, 768, 128, 8, 0, 0, 0) == 6
+    assert lib.moe_layer_kernel_count(5, 2048, 768, 128, 8, 0, 0, 0) == 6
     assert lib.moe_layer_kernel_count(4096, 2048, 768, 128, 8, 0, 0, 0) == 6
-    assert lib.moe_layer_kernel_count(1, 4096, 2048, 256, 6, 2, 1, 3) == 5
+    assert lib.moe_layer_kernel_count(1, 4096, 2048, 256, 6, 2, 1, 3) == 4
     assert lib.moe_layer_kernel_count(8, 4096, 2048, 256, 6, 2, 1, 3) == 7
     assert lib.moe_layer_kernel_count(4096, 4096, 2048, 256, 6, 2, 1, 3) == 7
-    assert lib.moe_layer_kernel_count(1, 2048, 768, 640, 8, 0, 0, 0) == 5
+    assert lib.moe_layer_kernel_count(1, 2048, 768, 640, 8, 0, 0, 0) == 4
     assert lib.moe_layer_kernel_count(0, 2048, 768, 128, 8, 0, 0, 0) == 0
     # a bf16 hidden with e2m1 experts adds the FP8 cast
     assert lib.moe_layer_kernel_count(4096, 4096, 2048, 256, 6, 0, 1, 3) == 8
