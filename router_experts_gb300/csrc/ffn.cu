@@ -78,17 +78,22 @@ struct Cfg {
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
 
-// Split count for the swap tiles: minimise (waves x k-blocks per unit) with a
-// per-unit overhead of one k-block, within the partial-sum capacity.  Lane l of
-// the calling warp evaluates s = l + 1 (every lane must call); ties go to the
-// fewest splits.  32-bit arithmetic: every product stays below 2^31.
+// Split count for the swap tiles: minimise waves x (k-blocks per unit + a
+// per-unit overhead), within the partial-sum capacity.  The overhead is
+// kSplitUnitCost k-blocks: a unit refills the operand pipeline from HBM and,
+// split, writes fp32 partials that the last split reads back, about 7 us
+// against about 0.5 us per k-block (fitted to GEMM1 times of the Qwen3 layer
+// at 1, 4 and 5 tokens; 14, 20 and 28 time alike).  Lane l of the calling warp
+// evaluates s = l + 1 (every lane must call); ties go to the fewest splits.
+// 32-bit arithmetic: every product stays below 2^31.
+constexpr int kSplitUnitCost = 14;
 MOE_DEV int choose_splits(int ug, int KB, int ctas, int max_slots) {
   const int lane = threadIdx.x & 31;
   const int s = lane + 1;
   uint32_t key = 0xFFFFFFFFu;
   if (ug > 0 && s <= KB && (s == 1 || ug * s <= max_slots)) {
     const int waves = (ug * s + ctas - 1) / ctas;
-    const int cost = waves * ((KB + s - 1) / s + 1);
+    const int cost = waves * ((KB + s - 1) / s + kSplitUnitCost);
     key = (static_cast<uint32_t>(min(cost, (1 << 26) - 1)) << 5) | static_cast<uint32_t>(lane);
   }
   key = __reduce_min_sync(0xffffffffu, key);
