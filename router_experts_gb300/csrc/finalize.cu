@@ -8,7 +8,8 @@
 // as 32-bit floats in slot order, round once to 16 bits).
 //
 // Memory-bound: one thread per 8 consecutive outputs (16-byte loads of each
-// of the token's k staged rows, one 16-byte store).
+// of the token's k staged rows, all issued before the first add when k <= 8,
+// one 16-byte store).
 #include "moe_common.cuh"
 #include "moe_internal.h"
 
@@ -16,6 +17,10 @@ namespace moe {
 
 namespace {
 
+// KMAX > 0: the k rows are loaded before any is added (k <= KMAX), so each
+// thread keeps k 16-byte loads in flight; KMAX = 0: any k, one row at a time.
+// Both add the rows in slot order, so their results are identical.
+template <int KMAX>
 __global__ void __launch_bounds__(256) finalize_kernel(const uint4* __restrict__ stage, int T,
                                                        int k, int H8, uint4* __restrict__ out) {
   const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -25,8 +30,7 @@ __global__ void __launch_bounds__(256) finalize_kernel(const uint4* __restrict__
   float acc[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-  for (int j = 0; j < k; ++j) {
-    const uint4 v = __ldg(stage + (t * k + j) * H8 + c);
+  auto add_row = [&](const uint4 v) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -35,6 +39,18 @@ __global__ void __launch_bounds__(256) finalize_kernel(const uint4* __restrict__
       acc[2 * i] += f.x;
       acc[2 * i + 1] += f.y;
     }
+  };
+  const uint4* row = stage + t * k * H8 + c;
+  if constexpr (KMAX > 0) {
+    uint4 v[KMAX];
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j)
+      if (j < k) v[j] = __ldg(row + static_cast<long long>(j) * H8);
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j)
+      if (j < k) add_row(v[j]);
+  } else {
+    for (int j = 0; j < k; ++j) add_row(__ldg(row + static_cast<long long>(j) * H8));
   }
   out[t * H8 + c] = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
                                pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
@@ -46,8 +62,12 @@ int launch_finalize(const void* stage, int T, int k, int H, void* out, cudaStrea
   const int H8 = H / 8;
   const long long n = static_cast<long long>(T) * H8;
   const int blocks = static_cast<int>((n + 255) / 256);
-  finalize_kernel<<<blocks, 256, 0, stream>>>(reinterpret_cast<const uint4*>(stage), T, k, H8,
-                                              reinterpret_cast<uint4*>(out));
+  const uint4* st = reinterpret_cast<const uint4*>(stage);
+  uint4* o = reinterpret_cast<uint4*>(out);
+  if (k <= 8)
+    finalize_kernel<8><<<blocks, 256, 0, stream>>>(st, T, k, H8, o);
+  else
+    finalize_kernel<0><<<blocks, 256, 0, stream>>>(st, T, k, H8, o);
   return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 
