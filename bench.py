@@ -197,7 +197,6 @@ class L2Flush:
 # capture of the same workload and kernel build (the profile that records it);
 # an entry is dropped whenever its kernel changes.
 MEASURED_TRAFFIC = {
-    ("qwen3", 4096, "ffn_gemm_kernel<0,128>"): (970.3e6, "profiles/ffn_gemm_qwen3_T4096.md"),
     ("v4lo", 4096, "lowbit_gemm_kernel<0>"): (2338.2e6, "profiles/lowbit_gemm_v4lo_T4096.md"),
 }
 
@@ -443,8 +442,12 @@ def run_ours(args):
     dom = max(names, key=lambda n: stage_ms[n])
     roof = roofline_of(st_model[dom]["bytes"], st_model[dom]["flops"], stage_ms[dom] / 1e3, peaks,
                        fp8=w.lowbit and dom in ("gemm1", "gemm2"))
+    # GEMM1 row tiles (BLOCK_M 128) gather the token rows with four warps up
+    # to H = 4096, with two otherwise (third template argument)
+    gw1 = 4 if (BM == 128 and H <= 4096) else 2
     gk = ("lowbit_gemm_kernel<%d>", "lowbit_gemm_kernel<%d>") if w.lowbit else \
-        ("ffn_gemm_kernel<%d," + str(BM) + ">", "ffn_gemm_kernel<%d," + str(BM) + ">")
+        ("ffn_gemm_kernel<%d," + str(BM) + "," + str(gw1) + ">",
+         "ffn_gemm_kernel<%d," + str(BM) + ",2>")
     roof["kernel"] = {"router": "router_kernel", "align": "align_kernel",
                       "gemm1": gk[0] % 0, "gemm2": gk[1] % 1,
                       "finalize": "finalize_kernel"}[dom]

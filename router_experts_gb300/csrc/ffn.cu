@@ -37,7 +37,8 @@ namespace moe {
 
 namespace {
 
-constexpr int kThreads = 256;
+// Warps: 0 TMA producer, 1 MMA issuer (+ TMEM), 2 .. 1+GW token-row gather
+// (GEMM1; idle in GEMM2), then four epilogue warps.
 constexpr int kBK = 64;                 // K elements per stage (128 bytes of bf16)
 constexpr int kStageBudget = 220 * 1024;
 
@@ -49,7 +50,7 @@ constexpr int kStageBudget = 220 * 1024;
 //   rows (GEMM1: 128 gate rows + the matching 128 up rows, two TMA boxes, so
 //   the epilogue pairs column c with column c + 128); one 128x256 MMA per K
 //   step; two 256-column accumulators, double-buffered.
-template <int KIND, int BM>
+template <int KIND, int BM, int GW = 2>
 struct Cfg {
   static constexpr bool SWAP = BM < 128;
   static constexpr bool GATHER = KIND == 0;
@@ -67,13 +68,15 @@ struct Cfg {
                                    : (2 * ACC_COLS <= 256) ? 256
                                                            : 512;
   static constexpr uint32_t IDESC = SWAP ? idesc_bf16_f32(128, BM) : idesc_bf16_f32(128, 256);
-  // gather: 16-byte chunks per gather thread per stage (64 threads, 8 chunks
-  // per 128-byte token row)
+  // gather: 16-byte chunks per gather thread per stage (32*GW threads, 8
+  // chunks per 128-byte token row)
+  static constexpr int G_THREADS = 32 * GW;
   static constexpr int G_ROWS = SWAP ? BM : 128;
-  static constexpr int G_PER_THREAD = G_ROWS / 8;
+  static constexpr int G_PER_THREAD = G_ROWS * 8 / G_THREADS;
+  static constexpr int THREADS = 64 + G_THREADS + 128;
   static constexpr int BAR_BYTES = 512;
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + BAR_BYTES;
-  static_assert(G_PER_THREAD >= 2 && G_ROWS % 8 == 0, "gather split");
+  static_assert(G_PER_THREAD >= 2 && (G_ROWS * 8) % G_THREADS == 0, "gather split");
   static_assert(STAGE_BYTES % 1024 == 0, "stage tiles must keep 1024-byte alignment");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
@@ -273,11 +276,11 @@ MOE_DEV void epilogue_rows128(const FfnParams& p, const Unit& u, int row, uint32
   }
 }
 
-template <int KIND, int BM>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int KIND, int BM, int GW>
+__global__ void __launch_bounds__(Cfg<KIND, BM, GW>::THREADS, 1)
     ffn_gemm_kernel(const __grid_constant__ CUtensorMap tm_w,
                     const __grid_constant__ CUtensorMap tm_in, const FfnParams p) {
-  using C = Cfg<KIND, BM>;
+  using C = Cfg<KIND, BM, GW>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -294,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::STAGES; ++i) {
-      mbar_init(&full_bar[i], 1 + (C::GATHER ? 64 : 0));
+      mbar_init(&full_bar[i], 1 + (C::GATHER ? C::G_THREADS : 0));
       mbar_init(&empty_bar[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -411,10 +414,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         umma_commit(&tfull_bar[buf]);
       }
     }
-  } else if (warp < 4) {
+  } else if (warp < 2 + GW) {
     // ---------------- token-row gather (GEMM1) ----------------
     if constexpr (C::GATHER) {
-      const int gt = threadIdx.x - 64;  // 0..63
+      const int gt = threadIdx.x - 64;  // 0 .. G_THREADS-1
       const int chunk = gt & 7;
       const __nv_bfloat16* x = reinterpret_cast<const __nv_bfloat16*>(p.x);
       const int nk = p.T * p.k;
@@ -426,7 +429,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t nbytes[C::G_PER_THREAD];
 #pragma unroll
         for (int i = 0; i < C::G_PER_THREAD; ++i) {
-          const int r = (gt >> 3) + 8 * i;
+          const int r = (gt >> 3) + (C::G_THREADS / 8) * i;
           const int a = row_assignment(p, u.b, BM, r);
           const bool valid = a >= 0 && a < nk;
           src[i] = valid ? x + static_cast<size_t>(a / p.k) * p.H + chunk * 8 : x;
@@ -442,7 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t tile = smem_u32(smem + st * C::STAGE_BYTES) + (C::SWAP ? C::A_BYTES : 0);
 #pragma unroll
           for (int i = 0; i < C::G_PER_THREAD; ++i) {
-            const int r = (gt >> 3) + 8 * i;
+            const int r = (gt >> 3) + (C::G_THREADS / 8) * i;
             const uint32_t dst = tile + r * 128 + ((chunk ^ (r & 7)) << 4);
             cp_async_16(dst, nbytes[i] ? src[i] + kb * kBK : src[i], nbytes[i]);
           }
@@ -455,9 +458,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ---------------- epilogue ----------------
-    const int ew = warp - 4;
+    const int ew = warp & 3;  // a warp reads the TMEM lane quarter warp % 4
     const int row = ew * 32 + lane;
-    const int et = threadIdx.x - 128;
+    const int et = row;
     uint32_t acc_it = 0;
     for (int uu = blockIdx.x; uu < sc.num_units; uu += gridDim.x, ++acc_it) {
       const Unit u = decode_unit<KIND, BM>(p, sc, uu);
@@ -607,23 +610,27 @@ bool make_map_e2m1(CUtensorMap* m, const void* base, uint64_t rows, uint64_t col
 
 namespace {
 
-template <int KIND, int BM>
+template <int KIND, int BM, int GW = 2>
 int launch_kind(const CUtensorMap& tw, const CUtensorMap& tin, const FfnParams& p, int num_sms,
                 cudaStream_t stream) {
-  using C = Cfg<KIND, BM>;
+  using C = Cfg<KIND, BM, GW>;
   static bool attr_set = false;
   if (!attr_set) {
-    if (cudaFuncSetAttribute(ffn_gemm_kernel<KIND, BM>,
+    if (cudaFuncSetAttribute(ffn_gemm_kernel<KIND, BM, GW>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::SMEM_BYTES) != cudaSuccess)
       return -1;
     attr_set = true;
   }
-  ffn_gemm_kernel<KIND, BM><<<num_sms, kThreads, C::SMEM_BYTES, stream>>>(tw, tin, p);
+  ffn_gemm_kernel<KIND, BM, GW><<<num_sms, C::THREADS, C::SMEM_BYTES, stream>>>(tw, tin, p);
   return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 
 }  // namespace
+
+// GEMM1 row tiles gather with four warps up to this H, with two above it
+// (measured per shape on GB300).
+constexpr int kGather4MaxH = 4096;
 
 int ffn_max_slots(int block_m) { return block_m == 16 ? 1024 : (block_m == 64 ? 256 : 0); }
 
@@ -657,6 +664,7 @@ int launch_ffn_gemm(int kind, int block_m, const void* w, const FfnParams& p, in
   if (kind == 0) {
     if (block_m == 16) rc = launch_kind<0, 16>(tw, tin, p, num_sms, stream);
     else if (block_m == 64) rc = launch_kind<0, 64>(tw, tin, p, num_sms, stream);
+    else if (p.H <= kGather4MaxH) rc = launch_kind<0, 128, 4>(tw, tin, p, num_sms, stream);
     else rc = launch_kind<0, 128>(tw, tin, p, num_sms, stream);
   } else {
     if (block_m == 16) rc = launch_kind<1, 16>(tw, tin, p, num_sms, stream);
