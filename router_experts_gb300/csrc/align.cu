@@ -9,8 +9,8 @@
 // with atomics (order within an expert varies run to run), this kernel places
 // them in ascending assignment id, so its output is unique.
 //
-// One cooperative launch of G CTAs (G grows with T*k, one CTA per 2048
-// assignments, at most 64), 16 warps each.  CTA c owns a contiguous segment
+// One cooperative launch of G CTAs (G grows with T*k, one CTA per 512
+// assignments, at most 16), 16 warps each.  CTA c owns a contiguous segment
 // of the assignments and warp w a contiguous piece of it.
 //   1. Count: each warp counts its piece into its shared-memory histogram row;
 //      a scan over the 16 rows gives each warp its base inside the CTA and the
@@ -36,7 +36,9 @@ namespace {
 
 constexpr int kAlignThreads = 512;
 constexpr int kAlignWarps = kAlignThreads / 32;
-constexpr int kAlignPerCta = 2048;  // assignments per CTA before another CTA is added
+constexpr int kAlignPerCta = 512;  // assignments per CTA before another CTA is added
+constexpr int kAlignGrid = 16;     // CTAs at most (more spend longer in the grid barrier)
+static_assert(kAlignGrid <= kAlignMaxCtas, "per-CTA histogram rows of the workspace");
 
 struct AlignArgs {
   const int32_t* ids;
@@ -321,7 +323,7 @@ int launch_align(const int32_t* topk_ids, int T, int k, int E, int block_m, int3
   a.E = E;
   a.BM = block_m;
   a.G = (a.n + kAlignPerCta - 1) / kAlignPerCta;
-  a.G = a.G < 1 ? 1 : (a.G > kAlignMaxCtas ? kAlignMaxCtas : a.G);
+  a.G = a.G < 1 ? 1 : (a.G > kAlignGrid ? kAlignGrid : a.G);
   a.seg = ((a.n + a.G - 1) / a.G + 31) / 32 * 32;
   // (align_few uses 98 words whatever E is)
   const size_t smem = align_smem_bytes(E) > 512 ? align_smem_bytes(E) : 512;

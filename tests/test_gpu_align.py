@@ -24,7 +24,7 @@ def run_both(ids, E, BM):
 
 
 @pytest.mark.parametrize("BM", [16, 64, 128])
-@pytest.mark.parametrize("T", [1, 8, 64, 512, 4096])
+@pytest.mark.parametrize("T", [1, 8, 64, 65, 512, 4096])
 def test_glm_shapes(T, BM):
     ids, _ = W.random_routing(T, 8, 288, seed=T + BM)
     run_both(ids, 288, BM)
@@ -33,7 +33,8 @@ def test_glm_shapes(T, BM):
 @pytest.mark.parametrize("T,k,E,BM,skew", [(16, 2, 8, 16, 0.0), (4096, 8, 128, 128, 0.0),
                                            (4096, 8, 256, 128, 1.1), (256, 8, 256, 64, 3.0),
                                            (1000, 6, 256, 64, 1.1), (4096, 8, 1024, 16, 0.5),
-                                           (3, 1, 4, 16, 0.0), (20000, 8, 64, 128, 2.0)])
+                                           (3, 1, 4, 16, 0.0), (20000, 8, 64, 128, 2.0),
+                                           (100, 6, 256, 64, 1.1), (2049, 8, 128, 64, 0.5)])
 def test_mixed(T, k, E, BM, skew):
     ids, _ = W.random_routing(T, k, E, seed=7, skew=skew)
     run_both(ids, E, BM)

@@ -66,12 +66,12 @@ def test_layer_is_deterministic():
 
 # The layer must equal the separate public calls (router, align, grouped FFN,
 # finalize) bit for bit: across the align kernel's one-CTA / many-CTA switch at
-# T*k = 2048, and at one token, where the layer skips the align launch and
+# T*k = 512, and at one token, where the layer skips the align launch and
 # uses single-assignment blocks (a token's experts are distinct, so these are
 # align's blocks).
 @pytest.mark.parametrize("name,T", [("qwen3", 1), ("qwen3", 2), ("qwen3", 3), ("qwen3", 13),
-                                    ("qwen3", 255), ("qwen3", 256), ("qwen3", 257), ("dsv3", 1),
-                                    ("dsv3", 2), ("dsv3", 256)])
+                                    ("qwen3", 64), ("qwen3", 65), ("qwen3", 255), ("qwen3", 256),
+                                    ("qwen3", 257), ("dsv3", 1), ("dsv3", 2), ("dsv3", 256)])
 def test_layer_equals_separate_calls(name, T):
     w = W.WORKLOADS[name]
     d = W.make_inputs(w, T, seed=11, device="cuda")
