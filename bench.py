@@ -197,6 +197,7 @@ class L2Flush:
 # capture of the same workload and kernel build (the profile that records it);
 # an entry is dropped whenever its kernel changes.
 MEASURED_TRAFFIC = {
+    ("qwen3", 4096, "ffn_gemm_kernel<0,128,4>"): (979.1e6, "profiles/ffn_gemm_qwen3_T4096.md"),
     ("v4lo", 4096, "lowbit_gemm_kernel<0>"): (2338.2e6, "profiles/lowbit_gemm_v4lo_T4096.md"),
 }
 
