@@ -327,13 +327,10 @@ int launch_align(const int32_t* topk_ids, int T, int k, int E, int block_m, int3
   a.seg = ((a.n + a.G - 1) / a.G + 31) / 32 * 32;
   // (align_few uses 98 words whatever E is)
   const size_t smem = align_smem_bytes(E) > 512 ? align_smem_bytes(E) : 512;
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(align_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(align_smem_bytes(kAlignMaxE))) != cudaSuccess)
-      return -1;
-    attr_set = true;
-  }
+  static std::atomic<unsigned long long> smem_set{0};
+  if (!ensure_smem_limit(reinterpret_cast<const void*>(align_kernel),
+                         static_cast<int>(align_smem_bytes(kAlignMaxE)), smem_set))
+    return -1;
   // the CTAs meet at a grid barrier: a cooperative launch guarantees that
   // all of them are resident at once (or fails to launch)
   cudaLaunchConfig_t cfg = {};

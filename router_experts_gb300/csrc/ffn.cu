@@ -614,14 +614,10 @@ template <int KIND, int BM, int GW = 2>
 int launch_kind(const CUtensorMap& tw, const CUtensorMap& tin, const FfnParams& p, int num_sms,
                 cudaStream_t stream) {
   using C = Cfg<KIND, BM, GW>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(ffn_gemm_kernel<KIND, BM, GW>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::SMEM_BYTES) != cudaSuccess)
-      return -1;
-    attr_set = true;
-  }
+  static std::atomic<unsigned long long> smem_set{0};
+  if (!ensure_smem_limit(reinterpret_cast<const void*>(ffn_gemm_kernel<KIND, BM, GW>),
+                         C::SMEM_BYTES, smem_set))
+    return -1;
   ffn_gemm_kernel<KIND, BM, GW><<<num_sms, C::THREADS, C::SMEM_BYTES, stream>>>(tw, tin, p);
   return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }

@@ -577,15 +577,12 @@ int launch_cast_e4m3(const void* x, int T, int H, uint8_t* codes, uint8_t* scale
 }
 
 int launch_lowbit_gemm(int kind, const LowbitParams& p, int num_sms, cudaStream_t stream) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(lowbit_gemm_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kMxSmem) != cudaSuccess ||
-        cudaFuncSetAttribute(lowbit_gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kMxSmem) != cudaSuccess)
-      return -1;
-    attr_set = true;
-  }
+  static std::atomic<unsigned long long> smem_set0{0}, smem_set1{0};
+  if (!ensure_smem_limit(reinterpret_cast<const void*>(lowbit_gemm_kernel<0>), kMxSmem,
+                         smem_set0) ||
+      !ensure_smem_limit(reinterpret_cast<const void*>(lowbit_gemm_kernel<1>), kMxSmem,
+                         smem_set1))
+    return -1;
   // packed weight codes [E*2F or E*H rows, K codes], box 128 codes x 64 rows;
   // the same bytes as a plain byte map (box 64 bytes x 64 rows) for the L2 warm-up
   const int K = (kind == 0) ? p.H : p.F;

@@ -8,6 +8,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace moe {
 
 // ---- fixed workspace header (offsets independent of shapes, so a workspace
@@ -24,6 +26,24 @@ constexpr int kAlignMaxE = 1024;
 constexpr size_t kWsHeaderBytes = kWsAlignHistOffset + 4ull * kAlignMaxCtas * kAlignMaxE;
 
 constexpr size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Raise a kernel's dynamic shared-memory limit on the current device, once per
+// device (the limit is an attribute of the function on each device, so a
+// process that drives several GPUs sets it on every one).  `done` is the
+// caller's per-kernel record of the devices already set (devices 0..63;
+// higher ones are set on every call).
+inline bool ensure_smem_limit(const void* kernel, int bytes,
+                              std::atomic<unsigned long long>& done) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  const unsigned long long bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+  if (bit != 0 && (done.load(std::memory_order_acquire) & bit) != 0) return true;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
+      cudaSuccess)
+    return false;
+  done.fetch_or(bit, std::memory_order_release);
+  return true;
+}
 
 // ---- router -----------------------------------------------------------------
 struct RouterPlan {

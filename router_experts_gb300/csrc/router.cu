@@ -677,13 +677,10 @@ int launch_tiled(RouterArgs a, int hidden_dt, int gate_dt, const RouterPlan& pla
                      static_cast<uint64_t>(p.planes) * E, H, p.nb))
     return -1;
   const int smem = p.stages * p.stage_bytes + 1024 + kRgBarBytes;
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(router_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kRgSmemBudget + 1024 + kRgBarBytes) != cudaSuccess)
-      return -1;
-    attr_set = true;
-  }
+  static std::atomic<unsigned long long> smem_set{0};
+  if (!ensure_smem_limit(reinterpret_cast<const void*>(router_gemm_kernel),
+                         kRgSmemBudget + 1024 + kRgBarBytes, smem_set))
+    return -1;
   router_gemm_kernel<<<dim3(plan.tnt, plan.tks), kRgThreads, smem, stream>>>(tm_x, tm_g, p);
   if (cudaGetLastError() != cudaSuccess) return -1;
   a.KS = plan.tks;
