@@ -16,8 +16,11 @@ Every function follows a passage of the pages (cited in ``moe_oracle.c``):
   * expert FFN -- "MoE Kernels, in depth" (naive per-expert loop, SwiGLU on
                   the fused gate/up matrix); "How GPUs Fuse Communication and
                   Computation During LLM Inference" §1.1 and §3.5.
-The whole layer has no printed end-to-end value on the pages: beyond the pins
-in ``tests/test_oracle_*.py`` its parity is "parity unpinned".
+The whole layer has no printed end-to-end value on the pages; its composition
+(router -> experts -> weighted combine) is pinned by hand-derived closed-form
+cases in ``tests/test_oracle_layer.py`` (grouped sigmoid routing with a bias,
+renormalisation and scaling; softmax routing with and without
+renormalisation).
 """
 from __future__ import annotations
 

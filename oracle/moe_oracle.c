@@ -17,8 +17,8 @@
  * Pins: every function here is checked by the CPU tests against values the
  * pages print (P1 Figures 1 and 3, the P2 moe_align_block_size worked example),
  * closed forms, brute force on tiny inputs and library casts.  The whole-layer
- * composition has no printed end-to-end value on the pages: its parity beyond
- * those pins is "parity unpinned".
+ * composition has no printed end-to-end value on the pages; it is pinned by
+ * hand-derived closed-form layers (logits ln of rationals, SwiGLU at +-ln 3).
  *
  * Conventions shared with the callers (plain C, no CUDA):
  *   dtype codes 0 = bf16, 1 = f32, 2 = FP8 e4m3 (+ one UE8M0 scale byte per 32
