@@ -523,39 +523,87 @@ def run_ours(args):
         del fl
 
     # ---- end to end through the public API, host buffers ----
+    # A serving loop: every step copies its hidden rows from pinned host
+    # memory, runs moe.layer and copies its output back to pinned host memory.
+    # With at least 1 MiB to copy per step the copies run on their own streams
+    # (one per direction, two device buffers each), so step i+1's input copy
+    # and step i-1's output copy overlap step i's layer; events order each
+    # buffer's reuse.  Smaller steps run the three in order on one stream (the
+    # cross-stream events would cost more than the copies they hide).
     x_host = d["hidden"].cpu().pin_memory()
-    y_host = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
-    x_dev = torch.empty_like(d["hidden"])
     xs_host = d["hidden_scale"].cpu().pin_memory() if w.lowbit else None
-    xs_dev = torch.empty_like(d["hidden_scale"]) if w.lowbit else None
-    lbe = dict(lbk, hidden_scale=xs_dev) if w.lowbit else {}
-    y_dev = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    y_host = [torch.empty((T, H), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    x_dev = [torch.empty_like(d["hidden"]) for _ in range(2)]
+    xs_dev = [torch.empty_like(d["hidden_scale"]) for _ in range(2)] if w.lowbit else None
+    y_dev = [torch.empty((T, H), dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    s_comp, s_in, s_out = (torch.cuda.Stream(dev) for _ in range(3))
+
+    h2d = x_host.numel() * x_host.element_size() + (xs_host.numel() if w.lowbit else 0)
+    overlap = h2d >= (1 << 20)
+
+    def serve(n):
+        """n steps; returns (start, end) events on the current stream."""
+        main = torch.cuda.current_stream(dev)
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        if not overlap:
+            t0.record(main)
+            for _ in range(n):
+                x_dev[0].copy_(x_host, non_blocking=True)
+                if w.lowbit:
+                    xs_dev[0].copy_(xs_host, non_blocking=True)
+                lbe = dict(lbk, hidden_scale=xs_dev[0]) if w.lowbit else {}
+                moe.layer(x_dev[0], d["gate"], d.get("bias"), d["w13"], d["w2"], k, w.scoring,
+                          w.n_group, w.topk_group, w.renormalize, w.scaling, ws=ws, out=y_dev[0],
+                          **lbe)
+                y_host[0].copy_(y_dev[0], non_blocking=True)
+            t1.record(main)
+            return t0, t1
+        landed = [torch.cuda.Event() for _ in range(2)]   # input of the buffer copied in
+        used = [torch.cuda.Event() for _ in range(2)]     # layer of the buffer done
+        taken = [torch.cuda.Event() for _ in range(2)]    # output of the buffer copied out
+        t0.record(main)
+        for st in (s_comp, s_in, s_out):
+            st.wait_event(t0)
+        for i in range(n):
+            b = i % 2
+            with torch.cuda.stream(s_in):
+                if i >= 2:
+                    s_in.wait_event(used[b])      # step i-2's layer has read x_dev[b]
+                x_dev[b].copy_(x_host, non_blocking=True)
+                if w.lowbit:
+                    xs_dev[b].copy_(xs_host, non_blocking=True)
+                landed[b].record(s_in)
+            with torch.cuda.stream(s_comp):
+                s_comp.wait_event(landed[b])
+                if i >= 2:
+                    s_comp.wait_event(taken[b])   # step i-2's output has left y_dev[b]
+                lbe = dict(lbk, hidden_scale=xs_dev[b]) if w.lowbit else {}
+                moe.layer(x_dev[b], d["gate"], d.get("bias"), d["w13"], d["w2"], k, w.scoring,
+                          w.n_group, w.topk_group, w.renormalize, w.scaling, ws=ws, out=y_dev[b],
+                          **lbe)
+                used[b].record(s_comp)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(used[b])
+                y_host[b].copy_(y_dev[b], non_blocking=True)
+                taken[b].record(s_out)
+        for st in (s_comp, s_in, s_out):
+            main.wait_stream(st)
+        t1.record(main)
+        return t0, t1
+
     K2 = max(3, min(K, 50))
-    for _ in range(2):
-        x_dev.copy_(x_host, non_blocking=True)
-        if w.lowbit:
-            xs_dev.copy_(xs_host, non_blocking=True)
-        moe.layer(x_dev, d["gate"], d.get("bias"), d["w13"], d["w2"], k, w.scoring, w.n_group,
-                  w.topk_group, w.renormalize, w.scaling, ws=ws, out=y_dev, **lbe)
-        y_host.copy_(y_dev, non_blocking=True)
+    serve(4)
     torch.cuda.synchronize()
     barrier(world, dev)
-    a = torch.cuda.Event(enable_timing=True)
-    b = torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(K2):
-        x_dev.copy_(x_host, non_blocking=True)
-        if w.lowbit:
-            xs_dev.copy_(xs_host, non_blocking=True)
-        moe.layer(x_dev, d["gate"], d.get("bias"), d["w13"], d["w2"], k, w.scoring, w.n_group,
-                  w.topk_group, w.renormalize, w.scaling, ws=ws, out=y_dev, **lbe)
-        y_host.copy_(y_dev, non_blocking=True)
-    b.record(stream)
+    a, b = serve(K2)
     torch.cuda.synchronize()
     e2e_ms = reduce_max(a.elapsed_time(b), world, dev)
-    h2d = x_host.numel() * x_host.element_size() + (xs_host.numel() if w.lowbit else 0)
     e2e = {"value": round(world * T * K2 / (e2e_ms / 1e3), 1), "unit": UNIT,
-           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": T * H * 2}
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": T * H * 2, "steps": K2,
+           "overlap": ("copies of neighbouring steps overlap the layer (copy stream per "
+                       "direction, two buffers each)") if overlap else
+                      "none (copy in, layer, copy out in order on one stream)"}
     code = moe.read_device_error(ws.buf)
 
     # ---- CPU oracle baseline (rank 0, N = 1 only) ----
