@@ -132,3 +132,46 @@ def test_emulate_fp8_requant_scale_rule():
     scale = 4.0  # 1000 / 448 = 2.23 -> next power of two
     q = torch.tensor(act_last / scale, dtype=torch.float64).to(torch.float8_e4m3fn).double().item()
     assert y[0, 0] == pytest.approx(torch.tensor(q * scale).to(torch.bfloat16).double().item())
+
+
+def test_lowbit_ffn_equals_f32_ffn_on_decoded_values():
+    # Low-bit experts ("How GPUs Fuse Communication and Computation During LLM
+    # Inference" §1.1: FP8 activations, FP4 weights, one UE8M0 scale per 32
+    # values along the contraction): the oracle's FP8 x FP4 FFN must equal its
+    # f32 FFN on the same values decoded here, independently of the oracle --
+    # e4m3 through torch's float8 cast, e2m1 from the OCP table, scales
+    # 2^(s-127) applied per 32 values of x along H, of w13 along H and of w2
+    # along F.  A scale read along the wrong axis or from the wrong block
+    # changes the result.
+    rng = np.random.default_rng(12)
+    T, H, F, E, k = 3, 64, 64, 3, 2
+    table = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+
+    def fp4(shape):
+        nib = rng.integers(0, 16, size=shape)
+        vals = table[nib & 7] * np.where(nib & 8, -1.0, 1.0)
+        packed = (nib[..., 0::2] | (nib[..., 1::2] << 4)).astype(np.uint8)
+        return packed, vals
+
+    def scales(shape):
+        return rng.integers(127 - 4, 127 + 2, size=shape).astype(np.uint8)
+
+    def apply(vals, sc):
+        return vals * np.repeat(np.ldexp(1.0, sc.astype(np.int64) - 127), 32, axis=-1)
+
+    x_codes = rng.integers(0, 0x7E, size=(T, H)).astype(np.uint8)   # finite, non-negative
+    x_codes[1] |= 0x80                                               # negative row
+    x_vals = torch.from_numpy(x_codes).view(torch.float8_e4m3fn).double().numpy()
+    x_sc = scales((T, H // 32))
+    w13_q, w13_v = fp4((E, 2 * F, H))
+    w13_sc = scales((E, 2 * F, H // 32))
+    w2_q, w2_v = fp4((E, H, F))
+    w2_sc = scales((E, H, F // 32))
+    ids = np.array([[0, 2], [1, 0], [2, 1]], np.int32)
+    wts = np.array([[0.75, 0.25], [0.5, 0.5], [1.0, 0.125]])
+    low = oracle.moe_ffn(x_codes, "e4m3", w13_q, w2_q, "e2m1", T, H, F, E, k, ids, wts,
+                         x_scale=x_sc, w13_scale=w13_sc, w2_scale=w2_sc)
+    ref = oracle.moe_ffn(f32(apply(x_vals, x_sc)), "f32", f32(apply(w13_v, w13_sc)),
+                         f32(apply(w2_v, w2_sc)), "f32", T, H, F, E, k, ids, wts)
+    assert np.allclose(low, ref, rtol=1e-12, atol=1e-12)
+    assert np.abs(ref).max() > 1.0  # not vacuous
