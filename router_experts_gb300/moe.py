@@ -80,7 +80,16 @@ def load():
 
 
 def _p(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    """Device pointer of a tensor argument.  The library reads every tensor as
+    a dense row-major CUDA buffer, so anything else is refused here instead of
+    reaching a kernel as a host address or in the wrong layout."""
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"expected a CUDA tensor, got one on {t.device}")
+    if not t.is_contiguous():
+        raise ValueError(f"expected a contiguous tensor, got strides {t.stride()}")
+    return ctypes.c_void_p(t.data_ptr())
 
 
 def _stream(device=None):

@@ -130,3 +130,13 @@ def test_layer_kernel_count(lib):
     assert lib.moe_layer_kernel_count(0, 2048, 768, 128, 8, 0, 0, 0) == 0
     # a bf16 hidden with e2m1 experts adds the FP8 cast
     assert lib.moe_layer_kernel_count(4096, 4096, 2048, 256, 6, 0, 1, 3) == 8
+
+
+def test_binding_refuses_host_tensors():
+    # every tensor is handed to the kernels as a device address: a host tensor
+    # is refused in the binding instead of reaching a kernel
+    import torch
+    from router_experts_gb300 import moe
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        moe._p(torch.zeros((4, 64), dtype=torch.bfloat16))
+    assert moe._p(None) is None

@@ -88,3 +88,13 @@ def test_layer_equals_separate_calls(name, T):
     assert moe.layer_kernel_count(T, w.H, w.F, w.E, w.k) == (5 if T == 1 else 6)
     assert torch.equal(y, y2)
     assert moe.read_device_error(moe.default_workspace("cuda").buf) == 0
+
+
+def test_layer_refuses_strided_tensors():
+    # the kernels read dense row-major buffers: a transposed view is refused
+    # before anything is launched
+    w = W.WORKLOADS["toy"]
+    d = W.make_inputs(w, 64, seed=3, device="cuda")
+    xt = d["hidden"].reshape(w.H, 64).t()  # [64, H] view, not contiguous
+    with pytest.raises(ValueError, match="contiguous"):
+        moe.layer(xt, d["gate"], None, d["w13"], d["w2"], w.k)
