@@ -114,6 +114,34 @@ def test_align_and_ffn_reject_bad_arguments(lib):
     assert lib.moe_finalize(P(4096), 0, 2, 64, P(4096), None) == 0  # T = 0
 
 
+def call_layer(lib, T=4, H=64, F=32, E=8, k=2, act_dt=0, gate_dt=0, w_dt=0, block_m=16,
+               out=1 << 12, ws=1 << 12, ws_bytes=1 << 30, hidden=1 << 12):
+    P = ctypes.c_void_p
+    return lib.moe_layer(P(hidden), act_dt, None, P(1 << 12), gate_dt, None, P(1 << 12), None,
+                         P(1 << 12), None, w_dt, T, H, F, E, k, 0, 1, 1, 1, ctypes.c_float(1.0),
+                         block_m, P(out) if out else None, P(ws), ws_bytes, None)
+
+
+@no_device
+def test_layer_and_cast_reject_bad_arguments(lib):
+    # every case fails host validation before anything is launched
+    assert call_layer(lib, k=9) == 1              # k > E
+    assert call_layer(lib, block_m=32) == 1       # tile height not in {16, 64, 128}
+    assert call_layer(lib, H=96) == 1             # H % 64 for the expert GEMMs
+    assert call_layer(lib, F=48) == 1             # F % 32
+    assert call_layer(lib, ws_bytes=1024) == 1    # workspace too small
+    assert call_layer(lib, ws=(1 << 12) + 8) == 1  # workspace not 256-byte aligned
+    assert call_layer(lib, out=0) == 1            # no output
+    assert call_layer(lib, w_dt=3) == 1           # e2m1 experts need H, F % 128
+    assert call_layer(lib, act_dt=1) == 2         # fp32 activations into the expert GEMMs
+    assert call_layer(lib, T=0) == 0              # T = 0 is a no-op
+    P = ctypes.c_void_p
+    assert lib.moe_cast_e4m3(P(1 << 12), 4, 48, P(1 << 12), P(1 << 12), None) == 1  # H % 32
+    assert lib.moe_cast_e4m3(P(1 << 12), -1, 64, P(1 << 12), P(1 << 12), None) == 1
+    assert lib.moe_cast_e4m3(P((1 << 12) + 2), 4, 64, P(1 << 12), P(1 << 12), None) == 1
+    assert lib.moe_cast_e4m3(P(1 << 12), 0, 64, P(1 << 12), P(1 << 12), None) == 0
+
+
 def test_layer_kernel_count(lib):
     # router launches (two for bf16 hidden and gate; one below 8 tokens for an
     # fp32 gate; conversion + GEMM + selection for e4m3 hidden with an fp32
