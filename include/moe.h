@@ -59,6 +59,19 @@ typedef enum {
 
 typedef enum { MOE_DT_BF16 = 0, MOE_DT_F32 = 1, MOE_DT_E4M3 = 2, MOE_DT_E2M1 = 3 } moe_dtype;
 
+/* Workspace header words a test may set (byte offsets from the workspace
+ * start; everything else in the header is the library's own):
+ *   MOE_WS_ALIGN_BARRIER_OFFSET  int32[2]: arrival counter and generation of
+ *                                the align kernel's grid barrier (0 at rest)
+ *   MOE_WS_WAIT_LIMIT_OFFSET     int64: when > 0, the align kernel's grid
+ *                                barrier gives up after this many SM clock
+ *                                cycles instead of about 2^32 (~2 s); a test
+ *                                hook that makes the bounded-wait expiry
+ *                                path cheap to exercise.  0 after
+ *                                moe_workspace_init. */
+#define MOE_WS_ALIGN_BARRIER_OFFSET 5120
+#define MOE_WS_WAIT_LIMIT_OFFSET 5376
+
 /* Bits of the device error word. */
 #define MOE_DEVERR_BAD_EXPERT_ID 1 /* an expert id outside [0,E) was skipped          */
 #define MOE_DEVERR_WAIT_TIMEOUT 2  /* a bounded in-kernel wait expired; outputs invalid */
@@ -113,6 +126,23 @@ int moe_router(const void* hidden, int hidden_dt, const uint8_t* hidden_scale, c
                float* topk_weights, void* ws, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * moe_router_cast_e4m3 -- the router on a bf16 hidden state that also writes
+ * the hidden rows' FP8 cast for low-bit experts.  [P4] §1.1: a small kernel
+ * converts the layer input to FP8, computes the scales and writes both
+ * together with the router's output.  Same arguments, rules, workspace and
+ * kernels as moe_router with hidden_dt BF16; the warp that selects token t
+ * also writes row t of
+ *   codes  [T,H] e4m3 (16-byte aligned) and scales [T,H/32] UE8M0,
+ * exactly the bytes moe_cast_e4m3 writes.  moe_layer uses this path for a
+ * bf16 hidden with e2m1 experts.
+ * ------------------------------------------------------------------------- */
+int moe_router_cast_e4m3(const void* hidden, const void* gate, int gate_dt, const float* bias,
+                         int T, int H, int E, int k, int scoring, int n_group, int topk_group,
+                         int renormalize, float scaling, int32_t* topk_ids, float* topk_weights,
+                         uint8_t* codes, uint8_t* scales, void* ws, size_t ws_bytes,
+                         void* stream);
+
+/* ---------------------------------------------------------------------------
  * moe_router_noalloc -- the router for callers that cannot allocate device
  * memory.  (No counterpart on the pages: it exists for this library's users.)
  *
@@ -134,15 +164,21 @@ int moe_router(const void* hidden, int hidden_dt, const uint8_t* hidden_scale, c
  *     T <= 262,144.  Larger problems are rejected with MOE_ERR_ARG before
  *     anything is launched (e.g. T = 4,096 fits for every E <= 512;
  *     T = 8,192 with E = 512 does not).
- *   - The array (about 8.3 MiB) exists on every GPU that loads the library,
- *     until the process exits.
- *   - The first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.
+ *   - The array (8 MiB of partial logits and 64 KiB of tickets) exists on
+ *     every GPU that loads the library, until the process exits.
+ *   - The array's device address is looked up (cudaGetSymbolAddress, with
+ *     the device current) by the first call in each CUDA context and cached
+ *     per device with the id of that context; a call made in another context
+ *     of the device (after cudaDeviceReset, or with a context of the
+ *     caller's own made current) looks it up again.  Make the first call in
+ *     a context before any stream capture.
  *   - Every call shares the one array and leaves its contents behind; each
  *     call clears the tickets it uses before launching.  Calls that overlap in
  *     time on the GPU (different streams, or several host threads) race on
  *     the array and produce wrong results: serialise them.
+ *   - No device-side errors are reported: the one-launch router kernel has
+ *     no waits and no input value it could flag, so there is no error word
+ *     to read (moe_read_device_error applies to caller workspaces only).
  * ------------------------------------------------------------------------- */
 #define MOE_ROUTER_NOALLOC_MAX_LOGIT_BYTES (8u << 20)
 int moe_router_noalloc(const void* hidden, int hidden_dt, const uint8_t* hidden_scale,
@@ -235,6 +271,9 @@ int moe_grouped_ffn(const void* x, const uint8_t* x_scale, int act_dt, const voi
  * round once to 16 bits).
  *   stage [T*k, H] bf16 (weights already applied), out [T, H] bf16:
  *   out[t, h] = bf16(sum_{j=0..k-1} stage[t*k + j, h]) summed in fp32.
+ *   The staged rows themselves are bf16 (moe_expert_gemm2 rounds each
+ *   weighted slot row once), so a layer output is rounded once per slot row
+ *   and once more after the fp32 sum.
  * ------------------------------------------------------------------------- */
 int moe_finalize(const void* stage, int T, int k, int H, void* out, void* stream);
 
@@ -259,9 +298,11 @@ int moe_cast_e4m3(const void* x, int T, int H, uint8_t* codes, uint8_t* scales, 
  * per expert").  act_dt/w_dt as for the expert GEMMs; the router reads
  * `hidden` (dequantised when E4M3).  out [T,H] bf16.
  * act_dt BF16 with w_dt E2M1 (hidden_scale ignored): the router reads the
- * bf16 rows and the experts read their FP8 cast (moe_cast_e4m3, enqueued
- * between align and GEMM1; [P4] §1.1 puts that cast in front of the fused
- * expert kernel); hidden must be 16-byte aligned.
+ * bf16 rows and the experts read their FP8 cast, the codes and scales of
+ * moe_cast_e4m3, which the router's selecting warps write next to each
+ * token's ids and weights ([P4] §1.1: the cast in front of the fused expert
+ * kernel writes them together with the router's output); hidden must be
+ * 16-byte aligned.
  * One token (T == 1) skips the align launch: its k experts are distinct, so
  * every block holds one assignment and the GEMMs read topk_ids as the block
  * table ([P2] "vLLM's Triton path": the naive block assignment of small
@@ -279,6 +320,23 @@ int moe_layer(const void* hidden, int act_dt, const uint8_t* hidden_scale, const
               int block_m, void* out, void* ws, size_t ws_bytes, void* stream);
 /* Tile height moe_layer uses for block_m = 0. */
 int moe_pick_block_m(int T, int k, int E);
+
+/* ---------------------------------------------------------------------------
+ * Floor probes (measurement only; they compute nothing of the method).
+ * [P1] §3.3 "The Floor": the least a router can cost is one kernel launch and
+ * one cold read of the gate weight, measured with kernels that do no useful
+ * work.
+ * moe_probe_empty: an empty kernel of `blocks` blocks of `threads` threads
+ *   (1 <= blocks <= 2^20, 1 <= threads <= 512).
+ * moe_probe_read: every thread of ceil(bytes/16/512) blocks of 512 threads
+ *   loads 16 bytes of p (device, 16-byte aligned; bytes a multiple of 16), so
+ *   the kernel reads the buffer once.  sink is one device int32 that is
+ *   written only if a loaded 16-byte word XORs to 0x9E3779B9 (it keeps the
+ *   loads from being removed; its value means nothing).
+ * MOE_ERR_ARG for invalid arguments.
+ * ------------------------------------------------------------------------- */
+int moe_probe_empty(int blocks, int threads, void* stream);
+int moe_probe_read(const void* p, size_t bytes, int32_t* sink, void* stream);
 
 /* ---------------------------------------------------------------------------
  * Utilities.

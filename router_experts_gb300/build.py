@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libmoe.so")
 SOURCES = ["api.cu", "router.cu", "align.cu", "ffn.cu", "lowbit.cu", "finalize.cu",
-           "router_noalloc.cu"]
+           "router_noalloc.cu", "probe.cu"]
 HEADERS = ["moe_common.cuh", "moe_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr"]

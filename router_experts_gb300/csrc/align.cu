@@ -48,6 +48,7 @@ struct AlignArgs {
   int* hist;  // [G][E]
   int* bar;
   int* err;
+  const long long* wait_limit;  // workspace test hook: barrier limit in cycles, 0 = default
   long long cap, nbc;
   int n, E, BM, G, seg;
 };
@@ -202,7 +203,7 @@ __global__ void __launch_bounds__(kAlignThreads) align_kernel(const AlignArgs a)
   // 2. totals and this CTA's base per expert
   if (a.G > 1) {
     // on a timed-out barrier the table is incomplete: write nothing
-    if (!grid_barrier(a.bar, a.G, a.err)) return;
+    if (!grid_barrier(a.bar, a.G, a.err, a.wait_limit ? __ldcg(a.wait_limit) : 0)) return;
     for (int e = tid; e < E; e += kAlignThreads) {
       int t = 0, b = 0;
       for (int c0 = 0; c0 < a.G; c0 += 8) {
@@ -307,9 +308,10 @@ __global__ void __launch_bounds__(kAlignThreads) align_kernel(const AlignArgs a)
 
 int launch_align(const int32_t* topk_ids, int T, int k, int E, int block_m, int32_t* sorted_ids,
                  int64_t cap_rows, int32_t* block_expert, int32_t* num_post_padded, int* hist,
-                 int* bar, int* err, cudaStream_t stream) {
+                 int* bar, int* err, const long long* wait_limit, cudaStream_t stream) {
   if (E > kAlignMaxE) return -1;
   AlignArgs a;
+  a.wait_limit = wait_limit;
   a.ids = topk_ids;
   a.sorted = sorted_ids;
   a.blk = block_expert;

@@ -106,11 +106,18 @@ static int* align_hist(void* ws) {
 static int* align_bar(void* ws) {
   return reinterpret_cast<int*>(static_cast<char*>(ws) + kWsAlignBarrierOffset);
 }
+static const long long* wait_limit_word(void* ws) {
+  return reinterpret_cast<const long long*>(static_cast<char*>(ws) + kWsWaitLimitOffset);
+}
+static_assert(kWsAlignBarrierOffset == MOE_WS_ALIGN_BARRIER_OFFSET, "header layout");
+static_assert(kWsWaitLimitOffset == MOE_WS_WAIT_LIMIT_OFFSET, "header layout");
 
 // ---- checks -------------------------------------------------------------------
-static int check_router(const void* hidden, int hidden_dt, const uint8_t* hidden_scale,
-                        const void* gate, int gate_dt, int T, int H, int E, int k, int scoring,
-                        int n_group, int topk_group) {
+// Host-side argument rules of the router (moe_router, moe_router_noalloc and
+// the router step of moe_layer).
+int check_router(const void* hidden, int hidden_dt, const uint8_t* hidden_scale,
+                 const void* gate, int gate_dt, int T, int H, int E, int k, int scoring,
+                 int n_group, int topk_group) {
   if (T < 0 || H <= 0 || E <= 0 || k <= 0) return MOE_ERR_ARG;
   if (k > E || k > 16 || E > 512 || H % 32 != 0) return MOE_ERR_ARG;
   if (T > 16 * kRouterMaxTiles) return MOE_ERR_ARG;
@@ -260,6 +267,29 @@ int moe_router(const void* hidden, int hidden_dt, const uint8_t* hidden_scale, c
   return MOE_OK;
 }
 
+int moe_router_cast_e4m3(const void* hidden, const void* gate, int gate_dt, const float* bias,
+                         int T, int H, int E, int k, int scoring, int n_group, int topk_group,
+                         int renormalize, float scaling, int32_t* topk_ids, float* topk_weights,
+                         uint8_t* codes, uint8_t* scales, void* ws, size_t ws_bytes,
+                         void* stream) {
+  int rc = check_router(hidden, MOE_DT_BF16, nullptr, gate, gate_dt, T, H, E, k, scoring,
+                        n_group, topk_group);
+  if (rc != MOE_OK) return rc;
+  if (T == 0) return MOE_OK;
+  if (!topk_ids || !topk_weights || !codes || !scales || !ws || !aligned(codes, 16))
+    return MOE_ERR_ARG;
+  if (ws_bytes < moe_router_workspace_bytes(T, H, E) || !aligned(ws, 256)) return MOE_ERR_ARG;
+  const RouterPlan plan = plan_router(T, H, E);
+  char* base = static_cast<char*>(ws);
+  if (launch_router(hidden, MOE_DT_BF16, nullptr, gate, gate_dt, bias, T, H, E, k, scoring,
+                    n_group, topk_group, renormalize, scaling, topk_ids, topk_weights,
+                    reinterpret_cast<float*>(base + kWsHeaderBytes),
+                    reinterpret_cast<int*>(base + kWsRouterTicketOffset), err_word(ws), plan,
+                    static_cast<cudaStream_t>(stream), codes, scales) != 0)
+    return launch_fail("router kernel");
+  return MOE_OK;
+}
+
 // ---- align --------------------------------------------------------------------
 size_t moe_align_workspace_bytes(void) { return kWsHeaderBytes; }
 
@@ -276,7 +306,7 @@ int moe_align(const int32_t* topk_ids, int T, int k, int E, int block_m, int32_t
   if (ws_bytes < kWsHeaderBytes || !aligned(ws, 256)) return MOE_ERR_ARG;
   if (launch_align(topk_ids, T, k, E, block_m, sorted_ids, cap_rows, block_expert,
                    num_post_padded, align_hist(ws), align_bar(ws), err_word(ws),
-                   static_cast<cudaStream_t>(stream)) != 0)
+                   wait_limit_word(ws), static_cast<cudaStream_t>(stream)) != 0)
     return launch_fail("align kernel");
   return MOE_OK;
 }
@@ -463,6 +493,23 @@ static bool layer_skips_align(int T, int k, int E) {
   return T == 1;
 }
 
+// ---- floor probes -----------------------------------------------------------------
+int moe_probe_empty(int blocks, int threads, void* stream) {
+  if (blocks < 1 || blocks > (1 << 20) || threads < 1 || threads > 512) return MOE_ERR_ARG;
+  if (launch_probe_empty(blocks, threads, static_cast<cudaStream_t>(stream)) != 0)
+    return launch_fail("probe kernel");
+  return MOE_OK;
+}
+
+int moe_probe_read(const void* p, size_t bytes, int32_t* sink, void* stream) {
+  if (!p || !sink || bytes < 16 || bytes % 16 != 0 || !aligned(p, 16) ||
+      bytes / 16 > (static_cast<size_t>(1) << 40))
+    return MOE_ERR_ARG;
+  if (launch_probe_read(p, bytes, sink, static_cast<cudaStream_t>(stream)) != 0)
+    return launch_fail("probe kernel");
+  return MOE_OK;
+}
+
 // ---- FP8 cast -------------------------------------------------------------------
 int moe_cast_e4m3(const void* x, int T, int H, uint8_t* codes, uint8_t* scales, void* stream) {
   if (T < 0 || H <= 0 || H % 32 != 0) return MOE_ERR_ARG;
@@ -485,10 +532,11 @@ int moe_layer_kernel_count(int T, int H, int F, int E, int k, int act_dt, int ga
                            int w_dt) {
   if (T <= 0 || H <= 0 || F <= 0 || E <= 0 || k <= 0) return 0;
   // router + align (none for single-assignment blocks), GEMM1, GEMM2,
-  // finalize (+ the FP8 cast of a bf16 hidden for e2m1 experts)
-  const int cast = (act_dt == MOE_DT_BF16 && w_dt == MOE_DT_E2M1) ? 1 : 0;
+  // finalize (the FP8 cast of a bf16 hidden for e2m1 experts rides in the
+  // router's selection launch)
+  (void)w_dt;
   const int align = layer_skips_align(T, k, E) ? 0 : 1;
-  return moe_router_kernel_count(T, H, E, act_dt, gate_dt) + align + 3 + cast;
+  return moe_router_kernel_count(T, H, E, act_dt, gate_dt) + align + 3;
 }
 
 int moe_layer(const void* hidden, int act_dt, const uint8_t* hidden_scale, const void* gate,
@@ -520,11 +568,15 @@ int moe_layer(const void* hidden, int act_dt, const uint8_t* hidden_scale, const
   int32_t* npp = reinterpret_cast<int32_t*>(base + L.npp);
   void* stage = base + L.stage;
   const RouterPlan plan = plan_router(T, H, E);
+  // a bf16 hidden for e2m1 experts: the router's selecting warps also write
+  // the rows' FP8 cast ("How GPUs Fuse ..." §1.1), so no separate cast launch
+  uint8_t* cq = cast_input ? reinterpret_cast<uint8_t*>(base + L.xq) : nullptr;
+  uint8_t* cs = cast_input ? reinterpret_cast<uint8_t*>(base + L.xs) : nullptr;
   if (launch_router(hidden, act_dt, hidden_scale, gate, gate_dt, bias, T, H, E, k, scoring,
                     n_group, topk_group, renormalize, scaling, ids, wts,
                     reinterpret_cast<float*>(base + L.router),
                     reinterpret_cast<int*>(base + kWsRouterTicketOffset), err_word(ws), plan,
-                    s) != 0)
+                    s, cq, cs) != 0)
     return launch_fail("router kernel");
   const int naive = layer_skips_align(T, k, E) ? 1 : 0;
   if (naive) {
@@ -534,21 +586,14 @@ int moe_layer(const void* hidden, int act_dt, const uint8_t* hidden_scale, const
     sorted = ids;
     npp = ids;
   } else if (launch_align(ids, T, k, E, block_m, sorted, L.cap, blk, npp, align_hist(ws),
-                          align_bar(ws), err_word(ws), s) != 0) {
+                          align_bar(ws), err_word(ws), wait_limit_word(ws), s) != 0) {
     return launch_fail("align kernel");
   }
   const FfnLayout FL = ffn_layout(T, F, E, k, block_m, true, ffn_dt);
   void* inter = base + L.ffn + FL.inter;
   if (ffn_dt == MOE_DT_E4M3) {
-    const void* xq = hidden;
-    const uint8_t* xs = hidden_scale;
-    if (cast_input) {
-      uint8_t* cq = reinterpret_cast<uint8_t*>(base + L.xq);
-      uint8_t* cs = reinterpret_cast<uint8_t*>(base + L.xs);
-      if (launch_cast_e4m3(hidden, T, H, cq, cs, s) != 0) return launch_fail("cast kernel");
-      xq = cq;
-      xs = cs;
-    }
+    const void* xq = cast_input ? static_cast<const void*>(cq) : hidden;
+    const uint8_t* xs = cast_input ? cs : hidden_scale;
     if (!xs || !w13_scale || !w2_scale) return MOE_ERR_ARG;
     uint8_t* iq = static_cast<uint8_t*>(inter);
     uint8_t* isc = iq + align_up(static_cast<size_t>(L.cap) * F, 256);

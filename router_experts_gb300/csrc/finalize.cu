@@ -5,7 +5,10 @@
 // "Mixture of Experts" (ops.moe_sum reduces the top-k axis of the [T, k, H]
 // cache; the routing weight was applied by the down GEMM) and "How GPUs Fuse
 // Communication and Computation During LLM Inference" §3.7 (add the k slots
-// as 32-bit floats in slot order, round once to 16 bits).
+// as 32-bit floats in slot order, round once to 16 bits).  The staged rows
+// are already bf16 (the down GEMM rounds each weighted slot row once), so an
+// output is rounded twice in all: once per slot row in the stage and once
+// here, after the fp32 sum.
 //
 // Memory-bound: one thread per 8 consecutive outputs (16-byte loads of each
 // of the token's k staged rows, all issued before the first add when k <= 8,

@@ -511,56 +511,14 @@ __global__ void __launch_bounds__(kMxThreads, 1)
 
 // FP8 cast of the layer input ("How GPUs Fuse ..." §1.1: a small kernel turns
 // the layer input into FP8 codes and writes the scales; the scale rule of
-// §3.5): bf16 x [T, H] -> e4m3 codes [T, H] and one UE8M0 byte per 32 values,
-// 2^s the smallest power of two with amax / 2^s <= 448 (s in [-127, 127]; 0
-// for an all-zero group), codes = e4m3(v / 2^s), nearest, ties to even,
-// saturating.  One thread per group of 32: 64 bytes in, 33 out.  s comes from
-// amax's binary exponent, not from a rounded quotient: amax = m * 2^e with m
-// in [0.5, 1) and 448 = 0.875 * 2^9, so amax <= 448 * 2^s exactly when
-// s >= e - 9 (m <= 0.875) or s >= e - 8 (m > 0.875).
+// §3.5): bf16 x [T, H] -> e4m3 codes [T, H] and one UE8M0 byte per 32 values
+// (cast_e4m3_group32).  One thread per group of 32: 64 bytes in, 33 out.
 __global__ void __launch_bounds__(256) cast_e4m3_kernel(const uint4* __restrict__ x,
                                                         long long groups, uint4* __restrict__ codes,
                                                         uint8_t* __restrict__ scales) {
   for (long long g = blockIdx.x * 256ll + threadIdx.x; g < groups;
-       g += static_cast<long long>(gridDim.x) * 256) {
-    uint4 raw[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) raw[i] = __ldg(x + 4 * g + i);
-    float v[32];
-    float amax = 0.f;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint32_t w[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        v[8 * i + 2 * j] = __uint_as_float(w[j] << 16);          // bf16 -> fp32, exact
-        v[8 * i + 2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
-      }
-    }
-#pragma unroll
-    for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
-    int s = 0;
-    if (amax > 0.f) {
-      int e;
-      const float m = frexpf(amax, &e);
-      s = (m <= 0.875f) ? e - 9 : e - 8;
-      s = max(-127, min(127, s));
-    }
-    // 2^-s exactly (2^127 at most; 2^-127 is the subnormal 0x00400000)
-    const float mul = (s <= 126) ? __int_as_float((127 - s) << 23) : __int_as_float(0x00400000);
-    uint32_t c[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(
-          make_float2(v[4 * i] * mul, v[4 * i + 1] * mul), __NV_SATFINITE, __NV_E4M3);
-      const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
-          make_float2(v[4 * i + 2] * mul, v[4 * i + 3] * mul), __NV_SATFINITE, __NV_E4M3);
-      c[i] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
-    }
-    codes[2 * g] = make_uint4(c[0], c[1], c[2], c[3]);
-    codes[2 * g + 1] = make_uint4(c[4], c[5], c[6], c[7]);
-    scales[g] = static_cast<uint8_t>(s + 127);
-  }
+       g += static_cast<long long>(gridDim.x) * 256)
+    cast_e4m3_group32(x + 4 * g, codes + 2 * g, scales + g);
 }
 
 }  // namespace

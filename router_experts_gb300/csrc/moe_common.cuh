@@ -5,6 +5,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -267,10 +268,12 @@ MOE_DEV void store_release_gpu(int* p, int v) {
 
 // Barrier over the CTAs of a cooperative launch (all co-resident).  bar[0]
 // counts arrivals and is reset by the last CTA, bar[1] is a generation that
-// the last CTA advances; both start at zero.  The wait is bounded: on expiry
-// it records kErrTimeout and returns false to every thread of the CTA (the
-// caller must then skip whatever depends on the other CTAs).
-MOE_DEV bool grid_barrier(int* bar, int nctas, int* err) {
+// the last CTA advances; both start at zero.  The wait is bounded: after
+// `limit` SM clock cycles (kWaitLimitCycles when limit <= 0) it records
+// kErrTimeout and returns false to every thread of the CTA (the caller must
+// then skip whatever depends on the other CTAs).
+MOE_DEV bool grid_barrier(int* bar, int nctas, int* err, long long limit = 0) {
+  if (limit <= 0) limit = kWaitLimitCycles;
   __shared__ int gb_ok;
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -284,7 +287,7 @@ MOE_DEV bool grid_barrier(int* bar, int nctas, int* err) {
     } else {
       const long long t0 = clock64();
       while (load_acquire_gpu(bar + 1) == gen) {
-        if (clock64() - t0 > kWaitLimitCycles) {
+        if (clock64() - t0 > limit) {
           raise_error(err, kErrTimeout);
           ok = 0;
           break;
@@ -331,6 +334,56 @@ MOE_DEV void st_global_v8(void* p, const uint32_t (&v)[8]) {
 MOE_DEV uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// FP8 cast of 32 consecutive bf16 values ("How GPUs Fuse Communication and
+// Computation During LLM Inference" §1.1 and the scale rule of §3.5): 2^s is
+// the smallest power of two with amax / 2^s <= 448 (s in [-127, 127]; 0 for
+// an all-zero group), codes = e4m3(v / 2^s), nearest, ties to even,
+// saturating; the scale byte is s + 127 (UE8M0).  s comes from amax's binary
+// exponent, not from a rounded quotient: amax = m * 2^e with m in [0.5, 1)
+// and 448 = 0.875 * 2^9, so amax <= 448 * 2^s exactly when s >= e - 9
+// (m <= 0.875) or s >= e - 8 (m > 0.875).  src: four 16-byte words (64
+// bytes), dst: two 16-byte words of codes.
+MOE_DEV void cast_e4m3_group32(const uint4* __restrict__ src, uint4* __restrict__ dst,
+                               uint8_t* __restrict__ scale) {
+  uint4 raw[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) raw[i] = __ldg(src + i);
+  float v[32];
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t w[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      v[8 * i + 2 * j] = __uint_as_float(w[j] << 16);  // bf16 -> fp32, exact
+      v[8 * i + 2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  int s = 0;
+  if (amax > 0.f) {
+    int e;
+    const float m = frexpf(amax, &e);
+    s = (m <= 0.875f) ? e - 9 : e - 8;
+    s = max(-127, min(127, s));
+  }
+  // 2^-s exactly (2^127 at most; 2^-127 is the subnormal 0x00400000)
+  const float mul = (s <= 126) ? __int_as_float((127 - s) << 23) : __int_as_float(0x00400000);
+  uint32_t c[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(
+        make_float2(v[4 * i] * mul, v[4 * i + 1] * mul), __NV_SATFINITE, __NV_E4M3);
+    const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
+        make_float2(v[4 * i + 2] * mul, v[4 * i + 3] * mul), __NV_SATFINITE, __NV_E4M3);
+    c[i] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+  }
+  dst[0] = make_uint4(c[0], c[1], c[2], c[3]);
+  dst[1] = make_uint4(c[4], c[5], c[6], c[7]);
+  *scale = static_cast<uint8_t>(s + 127);
 }
 
 }  // namespace moe

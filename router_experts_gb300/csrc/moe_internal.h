@@ -18,6 +18,7 @@ constexpr size_t kWsErrOffset = 0;                  // int32 sticky error word
 constexpr size_t kWsFfnTicketOffset = 1024;         // int32[kFfnMaxTickets]
 constexpr int kFfnMaxTickets = 1024;
 constexpr size_t kWsAlignBarrierOffset = 5120;      // int32[2] grid barrier of the align kernel
+constexpr size_t kWsWaitLimitOffset = 5376;         // int64 test hook: align barrier limit (cycles)
 constexpr size_t kWsRouterTicketOffset = 8192;      // int32[kRouterMaxTiles]
 constexpr int kRouterMaxTiles = 65536;              // token tiles of 16 -> T <= 1,048,576
 constexpr size_t kWsAlignHistOffset = kWsRouterTicketOffset + 4ull * kRouterMaxTiles;
@@ -63,20 +64,30 @@ struct RouterPlan {
 };
 // allow_tiled = false keeps every T on the fused kernel.
 RouterPlan plan_router(int T, int H, int E, bool allow_tiled = true);
+// Argument rules shared by every router entry point: MOE_OK, MOE_ERR_ARG or
+// MOE_ERR_UNSUPPORTED (the codes of include/moe.h).
+int check_router(const void* hidden, int hidden_dt, const uint8_t* hidden_scale, const void* gate,
+                 int gate_dt, int T, int H, int E, int k, int scoring, int n_group,
+                 int topk_group);
 // hidden_dt: 0 bf16, 1 f32, 2 e4m3; gate_dt: 0 bf16, 1 f32
 bool router_uses_tiled(const RouterPlan& plan, int hidden_dt, int gate_dt);
 int launch_router(const void* hidden, int hidden_dt, const uint8_t* hidden_scale,
                   const void* gate, int gate_dt, const float* bias, int T, int H, int E, int k,
                   int scoring, int n_group, int topk_group, int renormalize, float scaling,
                   int32_t* topk_ids, float* topk_weights, float* scratch, int* tickets, int* err,
-                  const RouterPlan& plan, cudaStream_t stream);
+                  const RouterPlan& plan, cudaStream_t stream, uint8_t* cast_codes = nullptr,
+                  uint8_t* cast_scales = nullptr);
+// cast_codes / cast_scales (bf16 hidden only, 16-byte aligned rows): the
+// selecting warp of every token also writes the token's FP8 cast ([T, H]
+// e4m3 codes, [T, H/32] UE8M0 scales), as moe_cast_e4m3 would.
 
 // ---- align ------------------------------------------------------------------
 // hist: int32[kAlignMaxCtas * kAlignMaxE] scratch; bar: int32[2], zero before
-// the first call (self-resetting afterwards).
+// the first call (self-resetting afterwards); wait_limit: the workspace's
+// barrier-limit word (nullptr or 0: the default limit).
 int launch_align(const int32_t* topk_ids, int T, int k, int E, int block_m, int32_t* sorted_ids,
                  int64_t cap_rows, int32_t* block_expert, int32_t* num_post_padded, int* hist,
-                 int* bar, int* err, cudaStream_t stream);
+                 int* bar, int* err, const long long* wait_limit, cudaStream_t stream);
 
 // ---- expert GEMMs -------------------------------------------------------------
 struct FfnParams {
@@ -127,6 +138,10 @@ int launch_cast_e4m3(const void* x, int T, int H, uint8_t* codes, uint8_t* scale
 
 // ---- finalize -----------------------------------------------------------------
 int launch_finalize(const void* stage, int T, int k, int H, void* out, cudaStream_t stream);
+
+// ---- floor probes (measurement) -------------------------------------------------
+int launch_probe_empty(int blocks, int threads, cudaStream_t stream);
+int launch_probe_read(const void* p, size_t bytes, int* sink, cudaStream_t stream);
 
 int device_num_sms();
 

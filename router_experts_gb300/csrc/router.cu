@@ -50,9 +50,28 @@ struct RouterArgs {
   int32_t* ids;
   float* wts;
   int* err;
+  // optional FP8 cast of the bf16 hidden rows, written by the selecting warp
+  // of each token next to its ids and weights (nullptr: none)
+  uint8_t* cast_codes;   // [T, H] e4m3
+  uint8_t* cast_scales;  // [T, H/32] UE8M0
   int T, H, E, k, scoring, n_group, topk_group, renorm, KS;
   float scaling;
 };
+
+// "How GPUs Fuse Communication and Computation During LLM Inference" §1.1:
+// the layer input's FP8 codes and scales are written together with the
+// router's outputs.  The warp that selected token t also casts its bf16 row
+// (one group of 32 values per lane at a time; cast_e4m3_group32).
+MOE_DEV void cast_token_row(const RouterArgs& a, int t) {
+  if (a.cast_codes == nullptr) return;
+  const int lane = threadIdx.x & 31;
+  const int G = a.H / 32;
+  const uint4* src = reinterpret_cast<const uint4*>(
+      reinterpret_cast<const __nv_bfloat16*>(a.x) + static_cast<size_t>(t) * a.H);
+  uint4* dst = reinterpret_cast<uint4*>(a.cast_codes + static_cast<size_t>(t) * a.H);
+  uint8_t* sc = a.cast_scales + static_cast<size_t>(t) * G;
+  for (int g = lane; g < G; g += 32) cast_e4m3_group32(src + 4 * g, dst + 2 * g, sc + g);
+}
 
 // Eight consecutive source values -> up to three bf16 parts, as four packed
 // bf16x2 registers per part (pairs (0,1), (2,3), (4,5), (6,7)).
@@ -403,7 +422,10 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(const RouterArgs
   for (int e = threadIdx.x; e < a.E; e += kRouterThreads)
     sbias[e] = a.bias ? __ldg(a.bias + e) : 0.f;
   __syncthreads();
-  for (int r = warp; r < rows; r += 8) select_dispatch(a, t0 + r, tile + r * a.E, sbias);
+  for (int r = warp; r < rows; r += 8) {
+    select_dispatch(a, t0 + r, tile + r * a.E, sbias);
+    cast_token_row(a, t0 + r);
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -587,6 +609,7 @@ __global__ void __launch_bounds__(kRouterThreads) router_select_kernel(const Rou
     if (lane + 32 * i < a.E) row[lane + 32 * i] = acc[i];
   __syncwarp();
   select_token<S>(a, t, row, sbias);
+  cast_token_row(a, t);
 }
 
 // Exact bf16 operands for the tiled gate GEMM: x e4m3 codes times their
@@ -735,8 +758,12 @@ int launch_router(const void* hidden, int hidden_dt, const uint8_t* hidden_scale
                   const void* gate, int gate_dt, const float* bias, int T, int H, int E, int k,
                   int scoring, int n_group, int topk_group, int renormalize, float scaling,
                   int32_t* topk_ids, float* topk_weights, float* scratch, int* tickets, int* err,
-                  const RouterPlan& plan, cudaStream_t stream) {
+                  const RouterPlan& plan, cudaStream_t stream, uint8_t* cast_codes,
+                  uint8_t* cast_scales) {
+  if (cast_codes != nullptr && (hidden_dt != 0 || cast_scales == nullptr)) return -2;
   RouterArgs a;
+  a.cast_codes = cast_codes;
+  a.cast_scales = cast_scales;
   a.x = hidden;
   a.x_scale = hidden_scale;
   a.gate = gate;

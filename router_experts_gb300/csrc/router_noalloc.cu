@@ -21,35 +21,75 @@
 
 namespace {
 
-constexpr size_t kErrBytes = 256;                        // error word, padded
 constexpr int kMaxTokenTiles = 16384;                    // tickets: T <= 262,144
 constexpr size_t kTicketBytes = 4ull * kMaxTokenTiles;   // 64 KiB
 constexpr size_t kLogitBytes = MOE_ROUTER_NOALLOC_MAX_LOGIT_BYTES;  // 8 MiB
-constexpr size_t kScratchBytes = kErrBytes + kTicketBytes + kLogitBytes;
+constexpr size_t kScratchBytes = kTicketBytes + kLogitBytes;
 
 static __device__ __align__(256) unsigned char g_router_noalloc_scratch[kScratchBytes];
 
-std::mutex g_mu;
-void* g_scratch_addr[64] = {};
+// The array's device address belongs to one CUDA context: after
+// cudaDeviceReset (or when the caller makes another context current) the
+// module is loaded again and the array may sit elsewhere.  The address is
+// therefore cached per device together with the unique id of the context it
+// was looked up in, and looked up again whenever the current context differs.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
 
-// Device address of the scratch array on the current device, looked up once
-// per device (host code only ever holds a host-side stand-in for the symbol,
-// so the address must come from the runtime).
+struct CachedAddress {
+  unsigned long long ctx_id;
+  void* addr;
+};
+
+std::mutex g_mu;
+CachedAddress g_cache[64] = {};
+CtxGetCurrentFn g_ctx_get_current = nullptr;
+CtxGetIdFn g_ctx_get_id = nullptr;
+
+// Unique id of the calling thread's current context (false if none is
+// current yet).  Called with g_mu held.
+bool current_context_id(unsigned long long* id) {
+  if (!g_ctx_get_current || !g_ctx_get_id) {
+    void* a = nullptr;
+    void* b = nullptr;
+    cudaDriverEntryPointQueryResult qa, qb;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &a, 12000, cudaEnableDefault, &qa) !=
+            cudaSuccess ||
+        qa != cudaDriverEntryPointSuccess ||
+        cudaGetDriverEntryPointByVersion("cuCtxGetId", &b, 12000, cudaEnableDefault, &qb) !=
+            cudaSuccess ||
+        qb != cudaDriverEntryPointSuccess)
+      return false;
+    g_ctx_get_current = reinterpret_cast<CtxGetCurrentFn>(a);
+    g_ctx_get_id = reinterpret_cast<CtxGetIdFn>(b);
+  }
+  CUcontext ctx = nullptr;
+  if (g_ctx_get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return false;
+  return g_ctx_get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+// Device address of the scratch array in the current device's current
+// context (host code only ever holds a host-side stand-in for the symbol, so
+// the address must come from the runtime).
 int scratch_address(void** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -1;
   std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_scratch_addr[dev]) {
+  unsigned long long id = 0;
+  const bool have_ctx = current_context_id(&id);
+  if (!have_ctx || g_cache[dev].addr == nullptr || g_cache[dev].ctx_id != id) {
     void* p = nullptr;
+    // (the lookup also makes the device's primary context current if no
+    // context was current yet)
     if (cudaGetSymbolAddress(&p, g_router_noalloc_scratch) != cudaSuccess || p == nullptr)
       return -1;
-    g_scratch_addr[dev] = p;
+    if (!current_context_id(&id)) return -1;
+    g_cache[dev].ctx_id = id;
+    g_cache[dev].addr = p;
   }
-  *out = g_scratch_addr[dev];
+  *out = g_cache[dev].addr;
   return 0;
 }
-
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
 
@@ -59,22 +99,11 @@ extern "C" int moe_router_noalloc(const void* hidden, int hidden_dt, const uint8
                                   int renormalize, float scaling, int32_t* topk_ids,
                                   float* topk_weights, void* stream) {
   // the same argument rules as moe_router
-  if (T < 0 || H <= 0 || E <= 0 || k <= 0) return MOE_ERR_ARG;
-  if (k > E || k > 16 || E > 512 || H % 32 != 0) return MOE_ERR_ARG;
-  if (scoring != MOE_SCORING_SOFTMAX && scoring != MOE_SCORING_SIGMOID &&
-      scoring != MOE_SCORING_SQRT_SOFTPLUS)
-    return MOE_ERR_ARG;
-  if (n_group < 1 || n_group > 32) return MOE_ERR_ARG;
-  if (n_group > 1 && (E % n_group != 0 || E / n_group < 2 || topk_group < 1 ||
-                      topk_group > n_group || topk_group * (E / n_group) < k))
-    return MOE_ERR_ARG;
-  if (hidden_dt != MOE_DT_BF16 && hidden_dt != MOE_DT_F32 && hidden_dt != MOE_DT_E4M3)
-    return MOE_ERR_UNSUPPORTED;
-  if (gate_dt != MOE_DT_BF16 && gate_dt != MOE_DT_F32) return MOE_ERR_UNSUPPORTED;
+  const int rc = moe::check_router(hidden, hidden_dt, hidden_scale, gate, gate_dt, T, H, E, k,
+                                   scoring, n_group, topk_group);
+  if (rc != MOE_OK) return rc;
   if (T == 0) return MOE_OK;
-  if (!hidden || !gate || !topk_ids || !topk_weights) return MOE_ERR_ARG;
-  if (hidden_dt == MOE_DT_E4M3 && !hidden_scale) return MOE_ERR_ARG;
-  if (!aligned16(hidden) || !aligned16(gate)) return MOE_ERR_ARG;
+  if (!topk_ids || !topk_weights) return MOE_ERR_ARG;
 
   // the static array bounds the problem size
   const moe::RouterPlan plan = moe::plan_router(T, H, E, false);
@@ -83,16 +112,15 @@ extern "C" int moe_router_noalloc(const void* hidden, int hidden_dt, const uint8
   void* base = nullptr;
   if (scratch_address(&base) != 0) return MOE_ERR_CUDA;
   char* b = static_cast<char*>(base);
-  int* err = reinterpret_cast<int*>(b);
-  int* tickets = reinterpret_cast<int*>(b + kErrBytes);
-  float* logits = reinterpret_cast<float*>(b + kErrBytes + kTicketBytes);
+  int* tickets = reinterpret_cast<int*>(b);
+  float* logits = reinterpret_cast<float*>(b + kTicketBytes);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
   // the array keeps the previous call's contents: the tickets must start at 0
   if (cudaMemsetAsync(tickets, 0, sizeof(int) * plan.nt, s) != cudaSuccess) return MOE_ERR_CUDA;
   if (moe::launch_router(hidden, hidden_dt, hidden_scale, gate, gate_dt, bias, T, H, E, k, scoring,
                          n_group, topk_group, renormalize, scaling, topk_ids, topk_weights, logits,
-                         tickets, err, plan, s) != 0)
+                         tickets, /*err=*/nullptr, plan, s) != 0)
     return MOE_ERR_CUDA;
   return MOE_OK;
 }

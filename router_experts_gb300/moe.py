@@ -20,6 +20,8 @@ SOFTMAX, SIGMOID, SQRT_SOFTPLUS = 0, 1, 2
 SCORING = {"softmax": SOFTMAX, "sigmoid": SIGMOID, "sqrt_softplus": SQRT_SOFTPLUS}
 DT_BF16, DT_F32, DT_E4M3, DT_E2M1 = 0, 1, 2, 3
 DEVERR_BAD_EXPERT_ID, DEVERR_WAIT_TIMEOUT, DEVERR_BAD_TABLE = 1, 2, 4
+# workspace header words a test may set (include/moe.h)
+WS_ALIGN_BARRIER_OFFSET, WS_WAIT_LIMIT_OFFSET = 5120, 5376
 
 _lock = threading.Lock()
 _lib = None
@@ -48,6 +50,8 @@ def load():
                             ctypes.c_size_t)
         sig = {
             "moe_router_workspace_bytes": (SZ, [I, I, I]),
+            "moe_router_cast_e4m3": (I, [P, P, I, P, I, I, I, I, I, I, I, I, F, P, P, P, P, P, SZ,
+                                         P]),
             "moe_router_kernel_count": (I, [I, I, I, I, I]),
             "moe_layer_kernel_count": (I, [I, I, I, I, I, I, I, I]),
             "moe_cast_e4m3": (I, [P, I, I, P, P, P]),
@@ -66,6 +70,8 @@ def load():
             "moe_layer": (I, [P, I, P, P, I, P, P, P, P, P, I, I, I, I, I, I, I, I, I, I, F, I, P, P,
                               SZ, P]),
             "moe_pick_block_m": (I, [I, I, I]),
+            "moe_probe_empty": (I, [I, I, P]),
+            "moe_probe_read": (I, [P, SZ, P, P]),
             "moe_workspace_init": (I, [P, SZ, P]),
             "moe_read_device_error": (I, [P, P, I, P]),
             "moe_status_string": (ctypes.c_char_p, [I]),
@@ -175,6 +181,18 @@ def cast_e4m3(x):
     return codes, scales
 
 
+def probe_empty(blocks: int = 1, threads: int = 512, device=None):
+    """Enqueue an empty kernel (the launch part of a router's floor)."""
+    _check(load().moe_probe_empty(int(blocks), int(threads), _stream(device)), "moe_probe_empty")
+
+
+def probe_read(t: torch.Tensor, sink: torch.Tensor):
+    """Enqueue a kernel whose threads each load 16 bytes of t (the whole
+    tensor once): the cold-read part of a router's floor."""
+    _check(load().moe_probe_read(_p(t), t.numel() * t.element_size(), _p(sink),
+                                 _stream(t.device)), "moe_probe_read")
+
+
 # ---- entry points ---------------------------------------------------------------
 
 def router(hidden, gate, bias, k, scoring="softmax", n_group=1, topk_group=1, renormalize=True,
@@ -196,6 +214,29 @@ def router(hidden, gate, bias, k, scoring="softmax", n_group=1, topk_group=1, re
                         buf.numel(), _stream(dev))
     _check(rc, "moe_router")
     return ids, wts
+
+
+def router_cast_e4m3(hidden, gate, bias, k, scoring="softmax", n_group=1, topk_group=1,
+                     renormalize=True, scaling=1.0, ws: Workspace | None = None):
+    """Router on a bf16 hidden that also writes its FP8 cast -> (topk_ids [T,k]
+    int32, topk_weights [T,k] float32, e4m3 codes [T,H] uint8, UE8M0 scales
+    [T,H/32] uint8)."""
+    lib = load()
+    T, H = hidden.shape
+    E = gate.shape[0]
+    dev = hidden.device
+    ids = torch.empty((T, k), dtype=torch.int32, device=dev)
+    wts = torch.empty((T, k), dtype=torch.float32, device=dev)
+    codes = torch.empty((T, H), dtype=torch.uint8, device=dev)
+    scales = torch.empty((T, H // 32), dtype=torch.uint8, device=dev)
+    ws = ws or default_workspace(dev)
+    buf = ws.get(lib.moe_router_workspace_bytes(T, H, E))
+    rc = lib.moe_router_cast_e4m3(_p(hidden), _p(gate), _dt(gate, None), _p(bias), T, H, E, k,
+                                  SCORING[scoring], n_group, topk_group, int(bool(renormalize)),
+                                  float(scaling), _p(ids), _p(wts), _p(codes), _p(scales),
+                                  _p(buf), buf.numel(), _stream(dev))
+    _check(rc, "moe_router_cast_e4m3")
+    return ids, wts, codes, scales
 
 
 def align(topk_ids, E, block_m, cap_rows=None, ws: Workspace | None = None):

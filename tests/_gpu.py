@@ -52,3 +52,51 @@ def rel_err(got, ref):
     ref = np.asarray(ref, dtype=np.float64)
     scale = np.abs(ref).max()
     return float(np.abs(got - ref).max() / (scale if scale > 0 else 1.0))
+
+
+def block_of_assignment(sorted_ids, npp, T, k):
+    """Row block (position // BLOCK_M is taken by the caller) of every
+    assignment: position of assignment a in sorted_ids, -1 if absent."""
+    s = np.asarray(sorted_ids[:npp])
+    pos = np.full(T * k, -1, dtype=np.int64)
+    real = s < T * k
+    pos[s[real]] = np.nonzero(real)[0]
+    return pos
+
+
+def covering_tokens(sorted_ids, npp, BM, T, k, prefer, n_min, seed=0):
+    """Tokens such that every row block below the padded length holds at least
+    one of their assignments (every block of an expert with assignments holds
+    a real row, so every block can be covered), preferring tokens marked in
+    `prefer`, topped up with random tokens to at least n_min.  Returns
+    (tokens sorted ascending, number of blocks)."""
+    s = np.asarray(sorted_ids)
+    nblk = npp // BM
+    rows = s[:nblk * BM].reshape(nblk, BM)
+    blk = block_of_assignment(s, npp, T, k) // BM
+    covered = np.zeros(nblk, dtype=bool)
+    chosen = set()
+    rng = np.random.default_rng(seed)
+    for b in range(nblk):
+        if covered[b]:
+            continue
+        cand = rows[b][rows[b] < T * k] // k
+        good = cand[prefer[cand]]
+        pool = good if good.size else cand
+        t = int(pool[rng.integers(pool.size)])
+        chosen.add(t)
+        covered[blk[t * k:(t + 1) * k]] = True
+    assert covered.all()
+    rest = np.setdiff1d(np.arange(T), np.fromiter(chosen, dtype=np.int64))
+    extra = max(0, min(n_min, T) - len(chosen))
+    if extra:
+        chosen.update(int(t) for t in rng.choice(rest, extra, replace=False))
+    return np.array(sorted(chosen), dtype=np.int32), nblk
+
+
+def blocks_covered(sorted_ids, npp, BM, T, k, tokens):
+    """Row blocks below the padded length that hold an assignment of `tokens`."""
+    blk = block_of_assignment(sorted_ids, npp, T, k) // BM
+    a = (np.asarray(tokens, dtype=np.int64)[:, None] * k + np.arange(k)[None, :]).reshape(-1)
+    b = blk[a]
+    return np.unique(b[b >= 0]).size

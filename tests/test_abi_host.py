@@ -156,8 +156,9 @@ def test_layer_kernel_count(lib):
     assert lib.moe_layer_kernel_count(4096, 4096, 2048, 256, 6, 2, 1, 3) == 7
     assert lib.moe_layer_kernel_count(1, 2048, 768, 640, 8, 0, 0, 0) == 4
     assert lib.moe_layer_kernel_count(0, 2048, 768, 128, 8, 0, 0, 0) == 0
-    # a bf16 hidden with e2m1 experts adds the FP8 cast
-    assert lib.moe_layer_kernel_count(4096, 4096, 2048, 256, 6, 0, 1, 3) == 8
+    # a bf16 hidden with e2m1 experts: the FP8 cast rides in the router's
+    # selection launch (no launch of its own)
+    assert lib.moe_layer_kernel_count(4096, 4096, 2048, 256, 6, 0, 1, 3) == 7
 
 
 def test_binding_refuses_host_tensors():
@@ -168,3 +169,23 @@ def test_binding_refuses_host_tensors():
     with pytest.raises(ValueError, match="CUDA tensor"):
         moe._p(torch.zeros((4, 64), dtype=torch.bfloat16))
     assert moe._p(None) is None
+
+
+def test_header_offsets_match_the_binding():
+    # the workspace header words a test may set, as moe.h defines them
+    from router_experts_gb300 import moe
+    src = open(os.path.join(ROOT, "include", "moe.h")).read()
+    defs = dict(re.findall(r"#define\s+(MOE_WS_\w+)\s+(\d+)", src))
+    assert int(defs["MOE_WS_ALIGN_BARRIER_OFFSET"]) == moe.WS_ALIGN_BARRIER_OFFSET
+    assert int(defs["MOE_WS_WAIT_LIMIT_OFFSET"]) == moe.WS_WAIT_LIMIT_OFFSET
+
+
+def test_probe_arguments_rejected_on_host(lib):
+    lib.moe_probe_empty.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
+    lib.moe_probe_read.argtypes = [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p,
+                                   ctypes.c_void_p]
+    assert lib.moe_probe_empty(0, 512, None) == 1
+    assert lib.moe_probe_empty(1, 1024, None) == 1
+    assert lib.moe_probe_read(None, 4096, None, None) == 1
+    # a size that is not a whole number of 16-byte loads
+    assert lib.moe_probe_read(ctypes.c_void_p(256), 4008, ctypes.c_void_p(512), None) == 1

@@ -1,7 +1,11 @@
-"""Host logic of bench.py: the byte/FLOP model, the roofline arithmetic and
-the max-over-ranks reduction across two gloo ranks (no GPU)."""
+"""Host logic of bench.py: the byte/FLOP model, the roofline arithmetic, the
+clock summary, the max-over-ranks reduction across two gloo ranks and the
+--gpus N replica launcher (no GPU)."""
+import json
 import os
 import socket
+import subprocess
+import sys
 
 import pytest
 import torch
@@ -39,6 +43,23 @@ def test_roofline_picks_binding_resource():
     # the binding resource moves with the faster tensor rate
     r = bench.roofline_of(1.5e9, 2e12, 1.0, peaks, fp8=True)
     assert r["bound"] == "hbm"
+    # an fp8 rate measured in the run replaces the nominal ratio
+    r = bench.roofline_of(1e3, 1e15, 2.0, dict(peaks, fp8_tflops=1600.0), fp8=True)
+    assert r["peak"] == 1600.0 and r["frac"] == pytest.approx(500.0 / 1600.0)
+    assert "measured" in r["tensor_dtype"]
+
+
+def test_clock_summary_window_and_reasons():
+    c = bench.ClockSampler("0")
+    c.max_mhz = 2070.0
+    # (host time, SM MHz, NVML clocks-event reasons, W): power cap at t = 2
+    c.samples = [(1.0, 2070.0, 0, 500.0), (2.0, 1900.0, 0x4, 1390.0), (3.0, 1950.0, 0, 1200.0),
+                 (9.0, 600.0, 0x8, 100.0)]
+    s = c.summary(1.5, 3.5)
+    assert s["samples"] == 2 and s["sm_mhz"] == pytest.approx(1925.0)
+    assert s["reasons"] == ["sw_power_cap"] and s["sm_max_mhz"] == 2070.0
+    assert c.summary()["reasons"] == ["hw_slowdown", "sw_power_cap"]
+    assert c.summary(10.0, 11.0)["samples"] == 0
 
 
 def test_lowbit_work_model_bytes():
@@ -88,3 +109,20 @@ def test_smi_index_honours_visible_devices(monkeypatch):
     assert bench.smi_index(1) == "7"
     monkeypatch.delenv("CUDA_VISIBLE_DEVICES")
     assert bench.smi_index(2) == "2"
+
+
+def test_gpus_flag_launches_replicas_without_torchrun():
+    # bench.py --gpus 2 outside torchrun starts two replica processes itself;
+    # --dry-run keeps them off the GPU (gloo), each reporting rank + 1 ms, and
+    # rank 0 prints the maximum over ranks
+    env = {k: v for k, v in os.environ.items()
+           if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK", "MASTER_ADDR", "MASTER_PORT")}
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--gpus", "2",
+                        "--dry-run", "--steps", "3", "--warmup", "3"],
+                       capture_output=True, text=True, timeout=300, env=env)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    out = json.loads(lines[0])
+    assert out["n_gpus"] == 2 and out["ms_per_step"] == 2.0 and out["scaling"] == "weak"

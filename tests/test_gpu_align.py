@@ -76,3 +76,56 @@ def test_bad_ids_are_flagged_not_written():
 def test_few_assignments(T, k, E, BM):
     ids, _ = W.random_routing(T, k, E, seed=T * 31 + E)
     run_both(ids, E, BM)
+
+
+def test_align_barrier_wait_expires_and_reports():
+    """The bounded-wait expiry path, made to run out on purpose without
+    faulting anything.  The align kernel's CTAs (a cooperative launch) meet at
+    one grid barrier in the workspace header.  Presetting its arrival counter
+    to a huge value means no CTA ever draws the last ticket, so the generation
+    never advances and every CTA's wait runs out.  The header's wait-limit
+    test hook shortens that wait to 2^21 SM cycles (about a millisecond).
+    Expected: MOE_DEVERR_WAIT_TIMEOUT in the error word, no output written
+    (the CTAs return before placing anything), and a correct align once the
+    header is zeroed again."""
+    lib = moe.load()
+    T, k, E, BM = 512, 8, 128, 64  # 4,096 assignments: 8 CTAs, so the barrier is used
+    ids, _ = W.random_routing(T, k, E, seed=21)
+    ids_d = ids.cuda()
+    cap = T * k + E * (BM - 1)
+    nbc = (cap + BM - 1) // BM
+    guard = 64
+    ws = moe.Workspace("cuda")
+    buf = ws.get(lib.moe_align_workspace_bytes())
+    marker = -7
+    sorted_all = torch.full((cap + 2 * guard,), marker, dtype=torch.int32, device="cuda")
+    blk_all = torch.full((nbc + 2 * guard,), marker, dtype=torch.int32, device="cuda")
+    npp_all = torch.full((1 + 2 * guard,), marker, dtype=torch.int32, device="cuda")
+    sorted_ids, blk, npp = sorted_all[guard:guard + cap], blk_all[guard:guard + nbc], \
+        npp_all[guard:guard + 1]
+    stream = moe._stream(ids_d.device)
+
+    def call():
+        return lib.moe_align(moe._p(ids_d), T, k, E, BM, moe._p(sorted_ids), cap, moe._p(blk),
+                             moe._p(npp), moe._p(buf), buf.numel(), stream)
+
+    bar = buf[moe.WS_ALIGN_BARRIER_OFFSET:moe.WS_ALIGN_BARRIER_OFFSET + 8].view(torch.int32)
+    limit = buf[moe.WS_WAIT_LIMIT_OFFSET:moe.WS_WAIT_LIMIT_OFFSET + 8].view(torch.int64)
+    bar[0] = 1 << 30
+    limit[0] = 1 << 21
+    assert call() == moe.MOE_OK
+    code = moe.read_device_error(buf)
+    print(f"align with a barrier that never opens: error word {code}")
+    assert code & moe.DEVERR_WAIT_TIMEOUT
+    assert (sorted_all == marker).all() and (blk_all == marker).all() and (npp_all == marker).all()
+    # the header zeroed again: a normal, correct align on the same workspace
+    assert lib.moe_workspace_init(moe._p(buf), buf.numel(), stream) == moe.MOE_OK
+    assert call() == moe.MOE_OK
+    so, bo, nppo = oracle.align(ids.numpy(), T, k, E, BM)
+    torch.cuda.synchronize()
+    assert moe.read_device_error(buf) == 0
+    assert int(npp.item()) == nppo
+    assert np.array_equal(sorted_ids.cpu().numpy(), so)
+    assert np.array_equal(blk.cpu().numpy(), bo)
+    assert (sorted_all[:guard] == marker).all() and (sorted_all[guard + cap:] == marker).all()
+    assert (blk_all[:guard] == marker).all() and (blk_all[guard + nbc:] == marker).all()

@@ -11,12 +11,16 @@ import oracle
 from router_experts_gb300 import moe
 from router_experts_gb300 import workloads as W
 
-from _gpu import LAYER_RTOL_BF16, compact_experts, host, rel_err, sample_tokens
+from _gpu import LAYER_RTOL_BF16, blocks_covered, compact_experts, covering_tokens, host, \
+    rel_err, sample_tokens
 
 pytestmark = pytest.mark.gpu
 
 
-def ffn_case(name, T, BM, skew=0.0, ntok=64, seed=1, ids=None):
+def ffn_case(name, T, BM, skew=0.0, ntok=64, seed=1, ids=None, cover=False):
+    """ntok >= T compares every token; cover=True picks at least ntok tokens
+    so that every row block of the align output holds one of their
+    assignments."""
     w = W.WORKLOADS[name]
     d = W.make_inputs(w, T, seed=seed, device="cuda")
     if ids is None:
@@ -28,7 +32,15 @@ def ffn_case(name, T, BM, skew=0.0, ntok=64, seed=1, ids=None):
     stage = moe.grouped_ffn(d["hidden"], d["w13"], d["w2"], w.k, BM, s, b, npp, wts_d)
     y = moe.finalize(stage, T, w.k)
     torch.cuda.synchronize()
-    tokens = sample_tokens(T, ntok, seed=seed)
+    s_h, npp_h = s.cpu().numpy(), int(npp.item())
+    nblk = npp_h // BM
+    if ntok >= T:
+        tokens = np.arange(T, dtype=np.int32)
+    elif cover:
+        tokens, nblk = covering_tokens(s_h, npp_h, BM, T, w.k, np.ones(T, dtype=bool), ntok,
+                                       seed=seed)
+    else:
+        tokens = sample_tokens(T, ntok, seed=seed)
     rows = ids.numpy()[tokens]
     w13h, w2h, rid, En = compact_experts(d["w13"], d["w2"], rows)
     xh = host(d["hidden"])[tokens]
@@ -36,23 +48,30 @@ def ffn_case(name, T, BM, skew=0.0, ntok=64, seed=1, ids=None):
                          wts.numpy()[tokens].astype(np.float64))
     got = y.float().cpu().numpy()[tokens]
     err = rel_err(got, ref)
-    print(f"{name} T={T} BM={BM} skew={skew}: rel max err {err:.2e}")
+    ncov = blocks_covered(s_h, npp_h, BM, T, w.k, tokens)
+    print(f"{name} T={T} BM={BM} skew={skew}: {len(tokens)} tokens, {ncov} of {nblk} row "
+          f"blocks, rel max err {err:.2e}")
     assert np.isfinite(got).all()
     assert err <= LAYER_RTOL_BF16
+    if cover or ntok >= T:
+        assert ncov == nblk
     return err
 
 
+# every token is compared (Qwen3 T = 4096 included: all 32,768 assignments)
 @pytest.mark.parametrize("name,T,BM", [("toy", 16, 16), ("toy", 16, 64), ("toy", 16, 128),
                                        ("qwen3", 1, 16), ("qwen3", 64, 16), ("qwen3", 64, 64),
                                        ("qwen3", 64, 128), ("qwen3", 512, 64),
                                        ("qwen3", 4096, 128), ("qwen3", 4096, 64)])
 def test_ffn_matches_oracle(name, T, BM):
-    ffn_case(name, T, BM)
+    ffn_case(name, T, BM, ntok=T)
 
 
-@pytest.mark.parametrize("name,T,BM", [("dsv3", 1, 16), ("dsv3", 256, 64), ("dsv3", 4096, 128)])
-def test_ffn_dsv3(name, T, BM):
-    ffn_case(name, T, BM, skew=1.1, ntok=16)
+# skewed routing on the 22.5 GB workload: tokens covering every row block
+@pytest.mark.parametrize("name,T,BM,ntok", [("dsv3", 1, 16, 1), ("dsv3", 256, 64, 64),
+                                            ("dsv3", 4096, 128, 256)])
+def test_ffn_dsv3(name, T, BM, ntok):
+    ffn_case(name, T, BM, skew=1.1, ntok=ntok, cover=True)
 
 
 @pytest.mark.parametrize("BM", [16, 128])

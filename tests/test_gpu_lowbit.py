@@ -12,8 +12,8 @@ import oracle
 from router_experts_gb300 import moe
 from router_experts_gb300 import workloads as W
 
-from _gpu import GAP_MIN, LAYER_RTOL_LOWBIT, compact_experts, host, oracle_router, rel_err, \
-    sample_tokens
+from _gpu import GAP_MIN, LAYER_RTOL_LOWBIT, WEIGHT_ATOL, blocks_covered, compact_experts, \
+    covering_tokens, host, oracle_router, rel_err, sample_tokens
 
 pytestmark = pytest.mark.gpu
 
@@ -39,8 +39,9 @@ def oracle_ffn_lowbit(d, tokens, ids_rows, w_rows, w, emulate=0):
                           w2_scale=s2, emulate=emulate)
 
 
-@pytest.mark.parametrize("T", [64, 512, 4096])
-def test_lowbit_ffn_matches_oracle(T):
+# T = 4096: at least 256 tokens covering every row block of the align output
+@pytest.mark.parametrize("T,ntok", [(64, 12), (512, 12), (4096, 256)])
+def test_lowbit_ffn_matches_oracle(T, ntok):
     w = W.WORKLOADS["v4lo"]
     d = v4lo_inputs(T, seed=2)
     ids, wts = W.random_routing(T, w.k, w.E, seed=T)
@@ -51,17 +52,26 @@ def test_lowbit_ffn_matches_oracle(T):
                             w2_scale=d["w2_scale"])
     y = moe.finalize(stage, T, w.k)
     torch.cuda.synchronize()
-    tokens = sample_tokens(T, 12, seed=T)
+    s_h, npp_h = s.cpu().numpy(), int(npp.item())
+    cover = ntok >= 256
+    if cover:
+        tokens, nblk = covering_tokens(s_h, npp_h, BM, T, w.k, np.ones(T, dtype=bool), ntok,
+                                       seed=T)
+    else:
+        tokens, nblk = sample_tokens(T, ntok, seed=T), npp_h // BM
     got = y.float().cpu().numpy()[tokens]
     ref = oracle_ffn_lowbit(d, tokens, ids.numpy()[tokens], wts.numpy()[tokens], w)
     err = rel_err(got, ref)
     emu = oracle_ffn_lowbit(d, tokens, ids.numpy()[tokens], wts.numpy()[tokens], w, emulate=2)
     err_emu = rel_err(got, emu)
-    print(f"low-bit ffn T={T} BM={BM}: rel err {err:.2e} (vs exact), {err_emu:.2e} (vs emulated "
-          f"re-quantisation)")
+    ncov = blocks_covered(s_h, npp_h, BM, T, w.k, tokens)
+    print(f"low-bit ffn T={T} BM={BM}: {len(tokens)} tokens, {ncov} of {nblk} row blocks, "
+          f"rel err {err:.2e} (vs exact), {err_emu:.2e} (vs emulated re-quantisation)")
     assert np.isfinite(got).all()
     assert err <= LAYER_RTOL_LOWBIT
     assert err_emu <= 2e-2
+    if cover:
+        assert ncov == nblk
 
 
 def test_lowbit_gemm_entry_points_compose():
@@ -85,25 +95,49 @@ def test_lowbit_gemm_entry_points_compose():
     assert codes.dtype == torch.uint8 and isc.dtype == torch.uint8
 
 
-# T = 1 runs with single-assignment blocks (no align launch)
-@pytest.mark.parametrize("T,ntok", [(1, 1), (8, 8), (512, 12), (4096, 12)])
+# T = 1 runs with single-assignment blocks (no align launch).  The oracle
+# routes every token (fp32 router inputs: the dequantised hidden rows and the
+# fp32 gate); at T = 4096 at least 256 tokens covering every row block are
+# compared, on the oracle's routing where the margin is clear and on the
+# GPU's for near-ties.
+@pytest.mark.parametrize("T,ntok", [(1, 1), (8, 8), (512, 12), (4096, 256)])
 def test_lowbit_layer_matches_oracle(T, ntok):
     w = W.WORKLOADS["v4lo"]
     d = v4lo_inputs(T, seed=0)
     y = moe.layer(d["hidden"], d["gate"], d["bias"], d["w13"], d["w2"], w.k, w.scoring,
                   renormalize=w.renormalize, scaling=w.scaling, hidden_scale=d["hidden_scale"],
                   w13_scale=d["w13_scale"], w2_scale=d["w2_scale"])
+    ids_d, wts_d = moe.router(d["hidden"], d["gate"], d["bias"], w.k, w.scoring,
+                              renormalize=w.renormalize, scaling=w.scaling,
+                              hidden_scale=d["hidden_scale"])
+    BM = moe.pick_block_m(T, w.k, w.E)
+    s, _, npp = moe.align(ids_d, w.E, BM)
     torch.cuda.synchronize()
-    tokens = sample_tokens(T, ntok, seed=T)
-    ids_o, w_o, gap = oracle_router(oracle, w, d, T, tokens)
-    keep = gap > GAP_MIN
-    tokens, ids_o, w_o = tokens[keep], ids_o[keep], w_o[keep]
-    ref = oracle_ffn_lowbit(d, tokens, ids_o, w_o, w)
+    ids_g, wts_g = ids_d.cpu().numpy(), wts_d.cpu().numpy().astype(np.float64)
+    s_h, npp_h = s.cpu().numpy(), int(npp.item())
+    ids_o, w_o, gap = oracle_router(oracle, w, d, T, np.arange(T, dtype=np.int32))
+    clear = gap > GAP_MIN
+    assert (ids_g[clear] == ids_o[clear]).all()
+    same = (ids_g == ids_o).all(axis=1)
+    assert np.abs(wts_g[same] - w_o[same]).max() <= WEIGHT_ATOL
+    cover = ntok >= 256
+    if cover:
+        tokens, nblk = covering_tokens(s_h, npp_h, BM, T, w.k, clear, ntok, seed=T)
+    else:
+        tokens, nblk = sample_tokens(T, ntok, seed=T), npp_h // BM
+    c = clear[tokens][:, None]
+    ids_t = np.where(c, ids_o[tokens], ids_g[tokens])
+    w_t = np.where(c, w_o[tokens], wts_g[tokens])
+    ref = oracle_ffn_lowbit(d, tokens, ids_t, w_t, w)
     got = y.float().cpu().numpy()[tokens]
     err = rel_err(got, ref)
-    print(f"low-bit layer T={T}: {len(tokens)} tokens, rel err {err:.2e}")
-    assert len(tokens) > 0 and np.isfinite(got).all()
+    ncov = blocks_covered(s_h, npp_h, BM, T, w.k, tokens)
+    print(f"low-bit layer T={T}: {len(tokens)} tokens ({int(c.sum())} on the oracle's routing), "
+          f"{ncov} of {nblk} row blocks, rel err {err:.2e}")
+    assert np.isfinite(got).all()
     assert err <= LAYER_RTOL_LOWBIT
+    if cover:
+        assert ncov == nblk
 
 
 def _shifted(t, off):
@@ -168,6 +202,37 @@ def test_cast_is_bit_exact_against_the_oracle():
     assert scales[2, 0].item() == 127 + 5 and scales[0, 0].item() == 127
 
 
+# The router's selection launch writes the FP8 cast next to the ids and
+# weights ("How GPUs Fuse ..." §1.1): codes and scales bit-exact against the
+# oracle's cast, ids and weights against the oracle's routing of the bf16 rows,
+# on both router paths (one launch below 8 tokens with an fp32 gate, tensor
+# cores from 8) and a bf16 gate.
+@pytest.mark.parametrize("T,gate_f32", [(1, True), (7, True), (8, True), (300, True),
+                                        (4096, True), (64, False)])
+def test_router_writes_the_fp8_cast(T, gate_f32):
+    w = W.WORKLOADS["v4lo"]
+    d = W.make_inputs(w, T, seed=6, device="cuda", experts=False)
+    g = torch.Generator(device="cuda").manual_seed(T + 1)
+    xb = torch.randn((T, w.H), generator=g, device="cuda", dtype=torch.float32).to(torch.bfloat16)
+    gate = d["gate"] if gate_f32 else d["gate"].to(torch.bfloat16)
+    ids, wts, codes, scales = moe.router_cast_e4m3(xb, gate, d["bias"], w.k, w.scoring,
+                                                   renormalize=w.renormalize, scaling=w.scaling)
+    torch.cuda.synchronize()
+    co, so = oracle.quantize_e4m3(host(xb), "bf16", T, w.H)
+    assert np.array_equal(codes.cpu().numpy(), co)
+    assert np.array_equal(scales.cpu().numpy(), so)
+    ids_o, w_o, gap = oracle.router(host(xb), "bf16", host(gate), "f32" if gate_f32 else "bf16",
+                                    d["bias"].cpu().numpy(), T, w.H, w.E, w.k, w.scoring,
+                                    renormalize=w.renormalize, scaling=w.scaling)
+    clear = gap > GAP_MIN
+    ids_h, wts_h = ids.cpu().numpy(), wts.cpu().numpy()
+    assert (ids_h[clear] == ids_o[clear]).all()
+    same = (ids_h == ids_o).all(axis=1)
+    assert np.abs(wts_h[same] - w_o[same]).max() <= WEIGHT_ATOL
+    print(f"router + FP8 cast T={T}: codes and scales bit-exact, {int(clear.sum())} tokens "
+          f"clear of the cut")
+
+
 @pytest.mark.parametrize("T,ntok", [(1, 1), (64, 16), (512, 12)])
 def test_bf16_input_lowbit_layer_matches_oracle(T, ntok):
     w = W.WORKLOADS["v4lo"]
@@ -179,8 +244,9 @@ def test_bf16_input_lowbit_layer_matches_oracle(T, ntok):
                   w2_scale=d["w2_scale"])
     torch.cuda.synchronize()
     align = 0 if T == 1 else 1
+    # router (+ the cast in its selection launch), align, GEMM1, GEMM2, finalize
     assert moe.layer_kernel_count(T, w.H, w.F, w.E, w.k, "bf16", "f32", "e2m1") == \
-        moe.router_kernel_count(T, w.H, w.E, "bf16", "f32") + 4 + align
+        moe.router_kernel_count(T, w.H, w.E, "bf16", "f32") + 3 + align
     tokens = sample_tokens(T, ntok, seed=T)
     # the router reads the bf16 rows; the experts read the oracle's own cast
     ids_o, w_o, gap = oracle.router(host(xb), "bf16", host(d["gate"]), "f32",
