@@ -557,6 +557,24 @@ class LayerBench:
         lg, _ = self.layer_graph(x, xs)
         tot = self.graph_us(lg, reps, flush)
         del lg, gs, ka
+        # the whole layer in one persistent kernel (small bf16 batches)
+        pers = None
+        if not w.lowbit and self.moe.layer_persistent_workspace_bytes(T, w.H, w.F, w.E, w.k):
+            torch = self.torch
+            wsp = self.moe.Workspace(self.dev)
+            out = torch.empty((T, w.H), dtype=torch.bfloat16, device=self.dev)
+            pa = self.layer_args(x)
+
+            def run_p():
+                self.moe.layer_persistent(pa[0], pa[1], pa[2], pa[3], pa[4], pa[5], pa[6], pa[7],
+                                          pa[8], pa[9], pa[10], ws=wsp, out=out)
+
+            run_p()
+            pg = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(pg):
+                run_p()
+            pers = self.graph_us(pg, reps, flush)
+            del pg, wsp
         sm_, lm = work_model(w, T, fs["touched"], fs["block_m"])
         lr = roofline_of(lm["bytes"], lm["flops"], tot / 1e6, self.peaks, fp8=w.lowbit)
         stage_roof = {}
@@ -564,13 +582,19 @@ class LayerBench:
             r = roofline_of(sm_[n]["bytes"], sm_[n]["flops"], us[n] / 1e6, self.peaks,
                             fp8=w.lowbit and n in ("gemm1", "gemm2"))
             stage_roof[n] = {"bound": r["bound"], "frac": round(r["frac"], 4)}
-        return {"us_per_layer": round(tot, 2), "tokens_per_s": round(T / (tot / 1e6), 1),
+        res = {"us_per_layer": round(tot, 2), "tokens_per_s": round(T / (tot / 1e6), 1),
                 "stage_us": {n: round(v, 2) for n, v in us.items()},
                 "stage_roofline": stage_roof,
                 "touched_experts": fs["touched"], "block_m": fs["block_m"],
                 "max_rows_per_expert": fs["max_rows"],
                 "roofline": {"bound": lr["bound"], "frac": round(lr["frac"], 4),
                              "achieved": round(lr["achieved"], 1), "unit": lr["unit"]}}
+        if pers is not None:
+            pr = roofline_of(lm["bytes"], lm["flops"], pers / 1e6, self.peaks)
+            res["persistent"] = {"us_per_layer": round(pers, 2),
+                                 "roofline": {"bound": pr["bound"], "frac": round(pr["frac"], 4)},
+                                 "note": "moe_layer_persistent: the whole layer in one kernel"}
+        return res
 
 
 def kernel_name(w, stage, BM, H):

@@ -322,6 +322,37 @@ int moe_layer(const void* hidden, int act_dt, const uint8_t* hidden_scale, const
 int moe_pick_block_m(int T, int k, int E);
 
 /* ---------------------------------------------------------------------------
+ * The whole layer in ONE persistent kernel, for small batches.  [P4] §3.3
+ * (GEMM 1 of an expert starts once its tokens are there, signalled by
+ * readiness counters), §3.4 (the fused kernel on a single GPU), §3.6 (GEMM 2
+ * tasks start before GEMM 1 has finished, waiting only for the rows they
+ * read).  The steps are the separate entry points': the one-launch router
+ * ([P1] §5.1, §5.3), the align with block_m 16 ([P3] Alignment), GEMM1 +
+ * SwiGLU and GEMM2 + routing weight ([P3] The fused expert GEMM) and the
+ * fixed-order combine ([P3] Combine), so the output equals moe_layer's up to
+ * the router's fp32 summation order.
+ *   Same arguments as moe_layer with every tensor bf16 (hidden [T,H], gate
+ *   [E,H], w13 [E,2F,H], w2 [E,H,F]; bias fp32 or NULL).  Limits: 1 <= T*k
+ *   <= 512, E <= 512, k <= 16, H % 64 == 0, F % 64 == 0, and the router's
+ *   expert tiles of 8 times its token tiles of 16 (ceil(E/8)*ceil(T/16)) at
+ *   most the GPU's SM count; MOE_ERR_ARG otherwise (nothing launched).
+ *   topk_ids [T,k] int32 / topk_weights [T,k] fp32: where the router's
+ *   selection goes (the caller may keep it, e.g. for expert-load statistics),
+ *   or both NULL to keep it in the workspace.
+ *   w13, w2, out 16-byte aligned; ws of moe_layer_persistent_workspace_bytes
+ *   (0 for shapes outside the limits), zeroed once before first use.
+ * One cooperative launch of one CTA per SM; every in-kernel wait (routing
+ * done, a block's GEMM1 rows ready) is bounded and sets
+ * MOE_DEVERR_WAIT_TIMEOUT on expiry.
+ * ------------------------------------------------------------------------- */
+size_t moe_layer_persistent_workspace_bytes(int T, int H, int F, int E, int k);
+int moe_layer_persistent(const void* hidden, const void* gate, const float* bias, const void* w13,
+                         const void* w2, int T, int H, int F, int E, int k, int scoring,
+                         int n_group, int topk_group, int renormalize, float scaling, void* out,
+                         int32_t* topk_ids, float* topk_weights, void* ws, size_t ws_bytes,
+                         void* stream);
+
+/* ---------------------------------------------------------------------------
  * Floor probes (measurement only; they compute nothing of the method).
  * [P1] §3.3 "The Floor": the least a router can cost is one kernel launch and
  * one cold read of the gate weight, measured with kernels that do no useful

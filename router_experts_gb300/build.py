@@ -17,8 +17,8 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libmoe.so")
 SOURCES = ["api.cu", "router.cu", "align.cu", "ffn.cu", "lowbit.cu", "finalize.cu",
-           "router_noalloc.cu", "probe.cu"]
-HEADERS = ["moe_common.cuh", "moe_internal.h"]
+           "router_noalloc.cu", "probe.cu", "decode.cu"]
+HEADERS = ["moe_common.cuh", "moe_internal.h", "router_device.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr"]
 

@@ -36,9 +36,9 @@ namespace {
 
 constexpr int kAlignThreads = 512;
 constexpr int kAlignWarps = kAlignThreads / 32;
-constexpr int kAlignPerCta = 512;  // assignments per CTA before another CTA is added
-constexpr int kAlignGrid = 16;     // CTAs at most (more spend longer in the grid barrier)
-static_assert(kAlignGrid <= kAlignMaxCtas, "per-CTA histogram rows of the workspace");
+// one CTA per 512 assignments, at most 16 (more spend longer in the grid
+// barrier): align_partition in moe_internal.h
+static_assert(16 <= kAlignMaxCtas, "per-CTA histogram rows of the workspace");
 
 struct AlignArgs {
   const int32_t* ids;
@@ -49,8 +49,10 @@ struct AlignArgs {
   int* bar;
   int* err;
   const long long* wait_limit;  // workspace test hook: barrier limit in cycles, 0 = default
+  int* ticket;                  // precounted: CTAs done reading hist
   long long cap, nbc;
   int n, E, BM, G, seg;
+  int precounted;               // hist already holds every CTA's counts (the router's)
 };
 
 MOE_DEV int warp_incl_scan(int v) {
@@ -197,13 +199,16 @@ __global__ void __launch_bounds__(kAlignThreads) align_kernel(const AlignArgs a)
       run += v;
     }
     base[e] = run;
-    if (a.G > 1) a.hist[static_cast<size_t>(c) * E + e] = run;
+    if (a.G > 1 && !a.precounted) a.hist[static_cast<size_t>(c) * E + e] = run;
   }
 
   // 2. totals and this CTA's base per expert
   if (a.G > 1) {
-    // on a timed-out barrier the table is incomplete: write nothing
-    if (!grid_barrier(a.bar, a.G, a.err, a.wait_limit ? __ldcg(a.wait_limit) : 0)) return;
+    // on a timed-out barrier the table is incomplete: write nothing.  With
+    // the router's counts the table is complete before the launch: no barrier
+    if (!a.precounted &&
+        !grid_barrier(a.bar, a.G, a.err, a.wait_limit ? __ldcg(a.wait_limit) : 0))
+      return;
     for (int e = tid; e < E; e += kAlignThreads) {
       int t = 0, b = 0;
       for (int c0 = 0; c0 < a.G; c0 += 8) {
@@ -219,6 +224,23 @@ __global__ void __launch_bounds__(kAlignThreads) align_kernel(const AlignArgs a)
       }
       tot[e] = t;
       base[e] = b;
+    }
+    {
+      // the last CTA to have read the table zeroes it, so it is all zeros
+      // between calls (the router of the next layer call adds its counts to
+      // it)
+      __syncthreads();
+      if (tid == 0) {
+        const int old = ticket_add_acq_rel(a.ticket, 1);
+        const int last = old == a.G - 1;
+        if (last) store_relaxed_gpu(a.ticket, 0);
+        wsum[0] = last;
+      }
+      __syncthreads();
+      if (wsum[0]) {
+        for (int i = tid; i < a.G * E; i += kAlignThreads) a.hist[i] = 0;
+      }
+      __syncthreads();
     }
   } else {
     for (int e = tid; e < E; e += kAlignThreads) {
@@ -308,10 +330,12 @@ __global__ void __launch_bounds__(kAlignThreads) align_kernel(const AlignArgs a)
 
 int launch_align(const int32_t* topk_ids, int T, int k, int E, int block_m, int32_t* sorted_ids,
                  int64_t cap_rows, int32_t* block_expert, int32_t* num_post_padded, int* hist,
-                 int* bar, int* err, const long long* wait_limit, cudaStream_t stream) {
+                 int* bar, int* err, const long long* wait_limit, cudaStream_t stream,
+                 bool precounted, int* ticket) {
   if (E > kAlignMaxE) return -1;
   AlignArgs a;
   a.wait_limit = wait_limit;
+  a.ticket = ticket;
   a.ids = topk_ids;
   a.sorted = sorted_ids;
   a.blk = block_expert;
@@ -324,9 +348,9 @@ int launch_align(const int32_t* topk_ids, int T, int k, int E, int block_m, int3
   a.n = T * k;
   a.E = E;
   a.BM = block_m;
-  a.G = (a.n + kAlignPerCta - 1) / kAlignPerCta;
-  a.G = a.G < 1 ? 1 : (a.G > kAlignGrid ? kAlignGrid : a.G);
-  a.seg = ((a.n + a.G - 1) / a.G + 31) / 32 * 32;
+  align_partition(a.n, &a.G, &a.seg);
+  a.precounted = (precounted && a.G > 1 && a.n > 32) ? 1 : 0;
+  if (a.G > 1 && ticket == nullptr) return -1;
   // (align_few uses 98 words whatever E is)
   const size_t smem = align_smem_bytes(E) > 512 ? align_smem_bytes(E) : 512;
   static std::atomic<unsigned long long> smem_set{0};

@@ -106,6 +106,9 @@ static int* align_hist(void* ws) {
 static int* align_bar(void* ws) {
   return reinterpret_cast<int*>(static_cast<char*>(ws) + kWsAlignBarrierOffset);
 }
+static int* align_ticket(void* ws) {
+  return reinterpret_cast<int*>(static_cast<char*>(ws) + kWsAlignTicketOffset);
+}
 static const long long* wait_limit_word(void* ws) {
   return reinterpret_cast<const long long*>(static_cast<char*>(ws) + kWsWaitLimitOffset);
 }
@@ -306,7 +309,8 @@ int moe_align(const int32_t* topk_ids, int T, int k, int E, int block_m, int32_t
   if (ws_bytes < kWsHeaderBytes || !aligned(ws, 256)) return MOE_ERR_ARG;
   if (launch_align(topk_ids, T, k, E, block_m, sorted_ids, cap_rows, block_expert,
                    num_post_padded, align_hist(ws), align_bar(ws), err_word(ws),
-                   wait_limit_word(ws), static_cast<cudaStream_t>(stream)) != 0)
+                   wait_limit_word(ws), static_cast<cudaStream_t>(stream), false,
+                   align_ticket(ws)) != 0)
     return launch_fail("align kernel");
   return MOE_OK;
 }
@@ -493,6 +497,45 @@ static bool layer_skips_align(int T, int k, int E) {
   return T == 1;
 }
 
+// ---- persistent layer for small batches ------------------------------------------
+size_t moe_layer_persistent_workspace_bytes(int T, int H, int F, int E, int k) {
+  if (T < 1 || H <= 0 || F <= 0 || E <= 0 || k <= 0) return 0;
+  const DecodePlan d = plan_decode(T, H, F, E, k, device_num_sms() > 0 ? device_num_sms() : 152);
+  return d.ok ? kWsHeaderBytes + d.bytes : 0;
+}
+
+int moe_layer_persistent(const void* hidden, const void* gate, const float* bias, const void* w13,
+                         const void* w2, int T, int H, int F, int E, int k, int scoring,
+                         int n_group, int topk_group, int renormalize, float scaling, void* out,
+                         int32_t* topk_ids, float* topk_weights, void* ws, size_t ws_bytes,
+                         void* stream) {
+  int rc = check_router(hidden, MOE_DT_BF16, nullptr, gate, MOE_DT_BF16, T, H, E, k, scoring,
+                        n_group, topk_group);
+  if (rc != MOE_OK) return rc;
+  if (T == 0) return MOE_OK;
+  if (F <= 0) return MOE_ERR_ARG;
+  // shape limits first (any SM count), then the plan for this GPU
+  if (!plan_decode(T, H, F, E, k, 1 << 20).ok) return MOE_ERR_ARG;
+  if (!w13 || !w2 || !out || !ws) return MOE_ERR_ARG;
+  if (!aligned(w13, 16) || !aligned(w2, 16) || !aligned(out, 16) || !aligned(ws, 256))
+    return MOE_ERR_ARG;
+  if ((topk_ids == nullptr) != (topk_weights == nullptr)) return MOE_ERR_ARG;
+  const int sms = device_num_sms();
+  if (sms <= 0) return cuda_fail("cudaDeviceGetAttribute", cudaGetLastError());
+  const DecodePlan d = plan_decode(T, H, F, E, k, sms);
+  if (!d.ok) return MOE_ERR_ARG;
+  if (ws_bytes < kWsHeaderBytes + d.bytes) return MOE_ERR_ARG;
+  char* base = static_cast<char*>(ws);
+  if (launch_decode_layer(hidden, gate, bias, w13, w2, T, H, F, E, k, scoring, n_group,
+                          topk_group, renormalize, scaling, out, topk_ids, topk_weights,
+                          base + kWsHeaderBytes,
+                          reinterpret_cast<int*>(base + kWsRouterTicketOffset),
+                          reinterpret_cast<int*>(base + kWsDecodeCounterOffset), err_word(ws),
+                          d, sms, static_cast<cudaStream_t>(stream)) != 0)
+    return launch_fail("persistent layer kernel");
+  return MOE_OK;
+}
+
 // ---- floor probes -----------------------------------------------------------------
 int moe_probe_empty(int blocks, int threads, void* stream) {
   if (blocks < 1 || blocks > (1 << 20) || threads < 1 || threads > 512) return MOE_ERR_ARG;
@@ -572,13 +615,19 @@ int moe_layer(const void* hidden, int act_dt, const uint8_t* hidden_scale, const
   // the rows' FP8 cast ("How GPUs Fuse ..." §1.1), so no separate cast launch
   uint8_t* cq = cast_input ? reinterpret_cast<uint8_t*>(base + L.xq) : nullptr;
   uint8_t* cs = cast_input ? reinterpret_cast<uint8_t*>(base + L.xs) : nullptr;
+  // with more than one align CTA, the router's selecting warps count the
+  // assignments of every align segment as they select ("How an MoE Model
+  // Picks Its Experts ..." §6.1), so the align launch needs no grid barrier
+  const int naive = layer_skips_align(T, k, E) ? 1 : 0;
+  int align_g = 1, align_seg = 0;
+  align_partition(T * k, &align_g, &align_seg);
+  const bool precount = !naive && align_g > 1 && T * k > 32;
   if (launch_router(hidden, act_dt, hidden_scale, gate, gate_dt, bias, T, H, E, k, scoring,
                     n_group, topk_group, renormalize, scaling, ids, wts,
                     reinterpret_cast<float*>(base + L.router),
                     reinterpret_cast<int*>(base + kWsRouterTicketOffset), err_word(ws), plan,
-                    s, cq, cs) != 0)
+                    s, cq, cs, precount ? align_hist(ws) : nullptr, align_seg) != 0)
     return launch_fail("router kernel");
-  const int naive = layer_skips_align(T, k, E) ? 1 : 0;
   if (naive) {
     // the GEMMs read the router's ids as the block table and need no other
     // align output (the pointers below are never dereferenced)
@@ -586,7 +635,8 @@ int moe_layer(const void* hidden, int act_dt, const uint8_t* hidden_scale, const
     sorted = ids;
     npp = ids;
   } else if (launch_align(ids, T, k, E, block_m, sorted, L.cap, blk, npp, align_hist(ws),
-                          align_bar(ws), err_word(ws), wait_limit_word(ws), s) != 0) {
+                          align_bar(ws), err_word(ws), wait_limit_word(ws), s, precount,
+                          align_ticket(ws)) != 0) {
     return launch_fail("align kernel");
   }
   const FfnLayout FL = ffn_layout(T, F, E, k, block_m, true, ffn_dt);

@@ -18,7 +18,9 @@ constexpr size_t kWsErrOffset = 0;                  // int32 sticky error word
 constexpr size_t kWsFfnTicketOffset = 1024;         // int32[kFfnMaxTickets]
 constexpr int kFfnMaxTickets = 1024;
 constexpr size_t kWsAlignBarrierOffset = 5120;      // int32[2] grid barrier of the align kernel
+constexpr size_t kWsAlignTicketOffset = 5128;       // int32 align: CTAs done reading the counts
 constexpr size_t kWsWaitLimitOffset = 5376;         // int64 test hook: align barrier limit (cycles)
+constexpr size_t kWsDecodeCounterOffset = 6144;     // int32[3] persistent layer: routed, zeroed, done
 constexpr size_t kWsRouterTicketOffset = 8192;      // int32[kRouterMaxTiles]
 constexpr int kRouterMaxTiles = 65536;              // token tiles of 16 -> T <= 1,048,576
 constexpr size_t kWsAlignHistOffset = kWsRouterTicketOffset + 4ull * kRouterMaxTiles;
@@ -76,18 +78,35 @@ int launch_router(const void* hidden, int hidden_dt, const uint8_t* hidden_scale
                   int scoring, int n_group, int topk_group, int renormalize, float scaling,
                   int32_t* topk_ids, float* topk_weights, float* scratch, int* tickets, int* err,
                   const RouterPlan& plan, cudaStream_t stream, uint8_t* cast_codes = nullptr,
-                  uint8_t* cast_scales = nullptr);
+                  uint8_t* cast_scales = nullptr, int* align_hist = nullptr, int align_seg = 0);
 // cast_codes / cast_scales (bf16 hidden only, 16-byte aligned rows): the
 // selecting warp of every token also writes the token's FP8 cast ([T, H]
 // e4m3 codes, [T, H/32] UE8M0 scales), as moe_cast_e4m3 would.
+// align_hist / align_seg: the selecting warp also adds each selected
+// assignment a = t*k + j to align_hist[(a / align_seg) * E + id] (the counts
+// launch_align takes with precounted = true).
 
 // ---- align ------------------------------------------------------------------
+// The align kernel's split of the n = T*k assignments: G CTAs (one per 512
+// assignments, 1..16), CTA c owning [c*seg, (c+1)*seg), seg a multiple of 32.
+inline void align_partition(int n, int* G, int* seg) {
+  int g = (n + 511) / 512;
+  g = g < 1 ? 1 : (g > 16 ? 16 : g);
+  *G = g;
+  *seg = ((n + g - 1) / g + 31) / 32 * 32;
+}
 // hist: int32[kAlignMaxCtas * kAlignMaxE] scratch; bar: int32[2], zero before
 // the first call (self-resetting afterwards); wait_limit: the workspace's
 // barrier-limit word (nullptr or 0: the default limit).
+// precounted: the router's selection already added every assignment to hist
+// ([G][E] of align_partition's segments), so the kernel skips publishing its
+// counts and the grid barrier.  Either way, with more than one CTA the last
+// CTA to have read hist zeroes it again (ticket: an int32, zero before the
+// first call, self-resetting), so hist is all zeros between calls.
 int launch_align(const int32_t* topk_ids, int T, int k, int E, int block_m, int32_t* sorted_ids,
                  int64_t cap_rows, int32_t* block_expert, int32_t* num_post_padded, int* hist,
-                 int* bar, int* err, const long long* wait_limit, cudaStream_t stream);
+                 int* bar, int* err, const long long* wait_limit, cudaStream_t stream,
+                 bool precounted = false, int* ticket = nullptr);
 
 // ---- expert GEMMs -------------------------------------------------------------
 struct FfnParams {
@@ -138,6 +157,28 @@ int launch_cast_e4m3(const void* x, int T, int H, uint8_t* codes, uint8_t* scale
 
 // ---- finalize -----------------------------------------------------------------
 int launch_finalize(const void* stage, int T, int k, int H, void* out, cudaStream_t stream);
+
+// ---- persistent decode layer (decode.cu) ----------------------------------------
+constexpr int kDecodeMaxAssignments = 512;  // T*k
+constexpr int kDecodeMaxSlots = 1024;       // split-K partial slots per GEMM (as ffn.cu, BM 16)
+struct DecodePlan {
+  bool ok;
+  int ne, nt, ks;  // router items: expert tiles of 8, token tiles of 16, K slices
+  size_t logits, ids, wts, ready, tokcnt, tick1, tick2, part1, part2, inter, stage, bytes;
+};
+// Shapes the persistent layer takes (bf16), the router's item split and the
+// layout of its workspace region (offsets from the region start).
+DecodePlan plan_decode(int T, int H, int F, int E, int k, int num_sms);
+// topk_ids / topk_weights: where the router writes (both nullptr: the
+// workspace region); region: d.bytes of workspace (zeroed once, left
+// reusable); router_tickets:
+// the header's router tickets; counters: int32[3] of the header (zeroed once).
+int launch_decode_layer(const void* hidden, const void* gate, const float* bias, const void* w13,
+                        const void* w2, int T, int H, int F, int E, int k, int scoring,
+                        int n_group, int topk_group, int renormalize, float scaling, void* out,
+                        int32_t* topk_ids, float* topk_weights, char* region,
+                        int* router_tickets, int* counters, int* err, const DecodePlan& d,
+                        int num_sms, cudaStream_t stream);
 
 // ---- floor probes (measurement) -------------------------------------------------
 int launch_probe_empty(int blocks, int threads, cudaStream_t stream);

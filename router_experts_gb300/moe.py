@@ -70,6 +70,9 @@ def load():
             "moe_layer": (I, [P, I, P, P, I, P, P, P, P, P, I, I, I, I, I, I, I, I, I, I, F, I, P, P,
                               SZ, P]),
             "moe_pick_block_m": (I, [I, I, I]),
+            "moe_layer_persistent_workspace_bytes": (SZ, [I, I, I, I, I]),
+            "moe_layer_persistent": (I, [P, P, P, P, P, I, I, I, I, I, I, I, I, I, F, P, P, P, P,
+                                         SZ, P]),
             "moe_probe_empty": (I, [I, I, P]),
             "moe_probe_read": (I, [P, SZ, P, P]),
             "moe_workspace_init": (I, [P, SZ, P]),
@@ -361,4 +364,36 @@ def layer(hidden, gate, bias, w13, w2, k, scoring="softmax", n_group=1, topk_gro
                        int(bool(renormalize)), float(scaling), block_m, _p(out), _p(buf),
                        buf.numel(), _stream(dev))
     _check(rc, "moe_layer")
+    return out
+
+
+def layer_persistent_workspace_bytes(T, H, F, E, k) -> int:
+    return int(load().moe_layer_persistent_workspace_bytes(T, H, F, E, k))
+
+
+def layer_persistent(hidden, gate, bias, w13, w2, k, scoring="softmax", n_group=1, topk_group=1,
+                     renormalize=True, scaling=1.0, ws: Workspace | None = None, out=None,
+                     routing=None):
+    """The whole layer in one persistent kernel (small batches, bf16) -> out
+    [T, H] bf16.  routing=(topk_ids [T,k] int32, topk_weights [T,k] f32): also
+    keep the router's selection there."""
+    lib = load()
+    T, H = hidden.shape
+    E = gate.shape[0]
+    F = w2.shape[2]
+    dev = hidden.device
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=dev) if out is None else out
+    if T == 0:
+        return out
+    need = lib.moe_layer_persistent_workspace_bytes(T, H, F, E, k)
+    if need == 0:
+        raise MoeError(MOE_ERR_ARG, "moe_layer_persistent_workspace_bytes")
+    ws = ws or default_workspace(dev)
+    buf = ws.get(need)
+    ids, wts = routing if routing is not None else (None, None)
+    rc = lib.moe_layer_persistent(_p(hidden), _p(gate), _p(bias), _p(w13), _p(w2), T, H, F, E, k,
+                                  SCORING[scoring], n_group, topk_group, int(bool(renormalize)),
+                                  float(scaling), _p(out), _p(ids), _p(wts), _p(buf), buf.numel(),
+                                  _stream(dev))
+    _check(rc, "moe_layer_persistent")
     return out

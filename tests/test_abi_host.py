@@ -189,3 +189,30 @@ def test_probe_arguments_rejected_on_host(lib):
     assert lib.moe_probe_read(None, 4096, None, None) == 1
     # a size that is not a whole number of 16-byte loads
     assert lib.moe_probe_read(ctypes.c_void_p(256), 4008, ctypes.c_void_p(512), None) == 1
+
+
+def test_persistent_layer_limits_checked_on_host(lib):
+    P, I = ctypes.c_void_p, ctypes.c_int
+    lib.moe_layer_persistent_workspace_bytes.restype = ctypes.c_size_t
+    lib.moe_layer_persistent_workspace_bytes.argtypes = [I, I, I, I, I]
+    fn = lib.moe_layer_persistent
+    fn.restype = I
+    fn.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, I, ctypes.c_float, P, P, P, P,
+                   ctypes.c_size_t, P]
+    # Qwen3 shapes: up to 64 tokens (T*k <= 512); F and H whole 64-wide K steps
+    assert lib.moe_layer_persistent_workspace_bytes(64, 2048, 768, 128, 8) > 0
+    assert lib.moe_layer_persistent_workspace_bytes(65, 2048, 768, 128, 8) == 0
+    assert lib.moe_layer_persistent_workspace_bytes(4, 2048, 96, 128, 8) == 0
+    assert lib.moe_layer_persistent_workspace_bytes(4, 2048, 768, 640, 8) == 0
+    a = P(1 << 12)
+    big = ctypes.c_size_t(1 << 40)
+    # nothing is launched for invalid arguments (the pointers are never read)
+    assert fn(a, a, None, a, a, 65, 2048, 768, 128, 8, 0, 1, 1, 1, 1.0, a, None, None, a, big,
+              None) == 1
+    assert fn(a, a, None, a, a, 4, 2048, 96, 128, 8, 0, 1, 1, 1, 1.0, a, None, None, a, big,
+              None) == 1
+    # ids without weights
+    assert fn(a, a, None, a, a, 4, 2048, 768, 128, 8, 0, 1, 1, 1, 1.0, a, a, None, a, big,
+              None) == 1
+    assert fn(a, a, None, a, a, 0, 2048, 768, 128, 8, 0, 1, 1, 1, 1.0, a, None, None, a, big,
+              None) == 0
