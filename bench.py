@@ -727,6 +727,12 @@ def run_ours(args):
             peaks["fp8_error"] = fp8_err
 
     w = W.WORKLOADS[args.workload]
+    if args.experts:
+        # fewer experts of the same shape: a smaller device footprint for
+        # profiler captures (the sweeps and the other workloads are skipped)
+        import dataclasses
+        w = dataclasses.replace(w, E=args.experts)
+        run_sweeps = False
     T = args.T
     k, E, H, F = w.k, w.E, w.H, w.F
     d = W.make_inputs(w, T, seed=args.seed, device=dev)
@@ -1107,6 +1113,9 @@ def main(argv=None):
     ap.add_argument("--cpu-tokens", type=int, default=0,
                     help="oracle sample size for cpu_baseline (0: about 15 s of CPU work)")
     ap.add_argument("--ref-tokens", type=int, default=64)
+    ap.add_argument("--experts", type=int, default=0,
+                    help="override the workload's expert count (profiler captures of a "
+                         "smaller device footprint; implies --no-sweep)")
     ap.add_argument("--traffic-csv", default="",
                     help="ncu --csv raw capture of this command's dominant kernel")
     ap.add_argument("--dry-run", action="store_true",

@@ -226,6 +226,11 @@ int moe_align(const int32_t* topk_ids, int T, int k, int E, int block_m, int32_t
  * moe_expert_gemm2: stage[a, h] = bf16(weight[a] * sum_f inter[p, f] * w2[e, h, f])
  *   for every real row p (a = sorted_ids[p] < T*k).
  * moe_grouped_ffn: both, with inter held in the workspace.
+ * Low-bit GEMM1 with a workspace of moe_ffn_workspace_bytes (and in
+ * moe_layer for an e4m3 hidden): one extra launch first copies x's rows (codes
+ * and scale bytes) into the blocks' padded order in the workspace, so the
+ * GEMM reads its token tiles by TMA; with a smaller workspace
+ * (moe_expert_gemm1 needs only the header) the GEMM gathers the rows itself.
  * w_dt must equal act_dt (BF16) or be E2M1 with act_dt E4M3 (low-bit).
  * Limits: H % 64 == 0, F % 32 == 0 (low-bit: H % 128 == 0, F % 128 == 0 and
  * every scale array 4-byte aligned), block_m in {16, 64, 128} (MOE_ERR_ARG

@@ -37,7 +37,7 @@ static bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_
 
 // ---- layouts ------------------------------------------------------------------
 struct FfnLayout {
-  size_t inter, partial, total;  // offsets from the region start
+  size_t inter, partial, xperm, xperm_scale, total;  // offsets from the region start
 };
 // The intermediate: bf16 [cap, F]; low-bit: e4m3 codes [cap, F] then UE8M0
 // scales [cap, F/32].
@@ -45,17 +45,26 @@ static size_t inter_bytes(size_t cap, int F, int act_dt) {
   if (act_dt == MOE_DT_E4M3) return align_up(cap * F, 256) + align_up(cap * (F / 32), 256);
   return align_up(cap * F * 2, 256);
 }
-static FfnLayout ffn_layout(int T, int F, int E, int k, int block_m, bool with_inter,
+// Low-bit: GEMM1's token rows permuted into the padded order (e4m3 codes
+// [cap, H] and scale bytes [cap, H/32]) follow the split-K partials.
+static FfnLayout ffn_layout(int T, int H, int F, int E, int k, int block_m, bool with_inter,
                             int act_dt = MOE_DT_BF16) {
   FfnLayout L{};
   size_t off = 0;
+  const size_t cap = static_cast<size_t>(T) * k + static_cast<size_t>(E) * (block_m - 1);
   if (with_inter) {
-    const size_t cap = static_cast<size_t>(T) * k + static_cast<size_t>(E) * (block_m - 1);
     L.inter = off;
     off += inter_bytes(cap, F, act_dt);
   }
   L.partial = off;
   off += ffn_partial_bytes(block_m);
+  L.xperm = L.xperm_scale = 0;
+  if (act_dt == MOE_DT_E4M3) {
+    L.xperm = off;
+    off += align_up(cap * H, 256);
+    L.xperm_scale = off;
+    off += align_up(cap * (H / 32), 256);
+  }
   L.total = off;
   return L;
 }
@@ -85,7 +94,7 @@ static LayerLayout layer_layout(int T, int H, int F, int E, int k, int block_m,
   L.router = off;
   off += plan_router(T, H, E).scratch_bytes;
   L.ffn = off;
-  off += ffn_layout(T, F, E, k, block_m, true, act_dt).total;
+  off += ffn_layout(T, H, F, E, k, block_m, true, act_dt).total;
   // a bf16 hidden may feed low-bit experts: room for its FP8 cast (the
   // low-bit intermediate is smaller than the bf16 one reserved above)
   L.xq = L.xs = 0;
@@ -319,7 +328,7 @@ int moe_align(const int32_t* topk_ids, int T, int k, int E, int block_m, int32_t
 size_t moe_ffn_workspace_bytes(int T, int H, int F, int E, int k, int block_m, int act_dt) {
   (void)H;
   if (T < 0 || F <= 0 || E <= 0 || k <= 0 || check_block_m(block_m) != MOE_OK) return 0;
-  return kWsHeaderBytes + ffn_layout(T, F, E, k, block_m, true, act_dt).total;
+  return kWsHeaderBytes + ffn_layout(T, H, F, E, k, block_m, true, act_dt).total;
 }
 
 // Low-bit path: kind 0 reads x codes/scales and writes the e4m3 intermediate
@@ -329,7 +338,8 @@ static int expert_gemm_lowbit(int kind, const void* act, const uint8_t* act_scal
                               int k, int block_m, const int32_t* sorted_ids,
                               const int32_t* block_expert, const int32_t* npp, int64_t cap_rows,
                               uint8_t* inter_q, uint8_t* inter_scale, const float* topk_weights,
-                              void* stage, void* ws, cudaStream_t stream, int naive = 0) {
+                              void* stage, void* ws, cudaStream_t stream, int naive = 0,
+                              uint8_t* xperm = nullptr, uint8_t* xperm_scale = nullptr) {
   if (!act || !act_scale || !w || !w_scale || !sorted_ids || !block_expert || !npp || !ws)
     return MOE_ERR_ARG;
   if (kind == 0 && (!inter_q || !inter_scale)) return MOE_ERR_ARG;
@@ -361,7 +371,8 @@ static int expert_gemm_lowbit(int kind, const void* act, const uint8_t* act_scal
   p.naive = naive;
   const int sms = device_num_sms();
   if (sms <= 0) return cuda_fail("cudaDeviceGetAttribute", cudaGetLastError());
-  if (launch_lowbit_gemm(kind, p, sms, stream) != 0) return launch_fail("low-bit GEMM kernel");
+  if (launch_lowbit_gemm(kind, p, sms, stream, xperm, xperm_scale) != 0)
+    return launch_fail("low-bit GEMM kernel");
   return MOE_OK;
 }
 
@@ -380,7 +391,7 @@ static int expert_gemm(int kind, const void* act, int act_dt, const void* w, int
   if (!aligned(ws, 256) || !aligned(act, 16) || !aligned(w, 16) || (inter && !aligned(inter, 32)) ||
       (stage && !aligned(stage, 32)))
     return MOE_ERR_ARG;
-  const FfnLayout L = ffn_layout(T, F, E, k, block_m, inter_in_ws);
+  const FfnLayout L = ffn_layout(T, H, F, E, k, block_m, inter_in_ws);
   if (ws_bytes < kWsHeaderBytes + L.total) return MOE_ERR_ARG;
   FfnParams p = ffn_params(T, H, F, E, k, block_m, sorted_ids, block_expert, npp, cap_rows, ws,
                            kWsHeaderBytes, L);
@@ -409,10 +420,18 @@ int moe_expert_gemm1(const void* x, int act_dt, const uint8_t* x_scale, const vo
     if (rc != MOE_OK) return rc;
     if (T == 0) return MOE_OK;
     if (ws_bytes < kWsHeaderBytes || !aligned(ws, 256)) return MOE_ERR_ARG;
+    // a workspace of moe_ffn_workspace_bytes holds the permuted token rows
+    // (read by TMA); a smaller one gets the gathering kernel
+    const FfnLayout L = ffn_layout(T, H, F, E, k, block_m, false, MOE_DT_E4M3);
+    const bool room = ws_bytes >= kWsHeaderBytes + L.total &&
+                      cap_rows <= static_cast<int64_t>(T) * k + static_cast<int64_t>(E) * (block_m - 1);
+    char* base = static_cast<char*>(ws) + kWsHeaderBytes;
     return expert_gemm_lowbit(0, x, x_scale, w13, w13_scale, T, H, F, E, k, block_m, sorted_ids,
                               block_expert, num_post_padded, cap_rows,
                               static_cast<uint8_t*>(inter), inter_scale, nullptr, nullptr, ws,
-                              static_cast<cudaStream_t>(stream));
+                              static_cast<cudaStream_t>(stream), 0,
+                              room ? reinterpret_cast<uint8_t*>(base + L.xperm) : nullptr,
+                              room ? reinterpret_cast<uint8_t*>(base + L.xperm_scale) : nullptr);
   }
   return expert_gemm(0, x, act_dt, w13, w_dt, T, H, F, E, k, block_m, sorted_ids, block_expert,
                      num_post_padded, cap_rows, inter, nullptr, nullptr, ws, ws_bytes, false,
@@ -452,15 +471,17 @@ int moe_grouped_ffn(const void* x, const uint8_t* x_scale, int act_dt, const voi
   if (ws_bytes < moe_ffn_workspace_bytes(T, H, F, E, k, block_m, act_dt)) return MOE_ERR_ARG;
   if (cap_rows != static_cast<int64_t>(T) * k + static_cast<int64_t>(E) * (block_m - 1))
     return MOE_ERR_ARG;  // the workspace holds exactly the worst-case intermediate
-  const FfnLayout L = ffn_layout(T, F, E, k, block_m, true, act_dt);
+  const FfnLayout L = ffn_layout(T, H, F, E, k, block_m, true, act_dt);
   void* inter = static_cast<char*>(ws) + kWsHeaderBytes + L.inter;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (act_dt == MOE_DT_E4M3) {
     uint8_t* iq = static_cast<uint8_t*>(inter);
     uint8_t* isc = iq + align_up(static_cast<size_t>(cap_rows) * F, 256);
+    char* region = static_cast<char*>(ws) + kWsHeaderBytes;
     rc = expert_gemm_lowbit(0, x, x_scale, w13, w13_scale, T, H, F, E, k, block_m, sorted_ids,
                             block_expert, num_post_padded, cap_rows, iq, isc, nullptr, nullptr,
-                            ws, s);
+                            ws, s, 0, reinterpret_cast<uint8_t*>(region + L.xperm),
+                            reinterpret_cast<uint8_t*>(region + L.xperm_scale));
     if (rc != MOE_OK) return rc;
     return expert_gemm_lowbit(1, iq, isc, w2, w2_scale, T, H, F, E, k, block_m, sorted_ids,
                               block_expert, num_post_padded, cap_rows, nullptr, nullptr,
@@ -576,10 +597,11 @@ int moe_layer_kernel_count(int T, int H, int F, int E, int k, int act_dt, int ga
   if (T <= 0 || H <= 0 || F <= 0 || E <= 0 || k <= 0) return 0;
   // router + align (none for single-assignment blocks), GEMM1, GEMM2,
   // finalize (the FP8 cast of a bf16 hidden for e2m1 experts rides in the
-  // router's selection launch)
-  (void)w_dt;
+  // router's selection launch; an e4m3 hidden's rows are permuted into the
+  // blocks' padded order by one more launch in front of GEMM1)
   const int align = layer_skips_align(T, k, E) ? 0 : 1;
-  return moe_router_kernel_count(T, H, E, act_dt, gate_dt) + align + 3;
+  const int perm = (act_dt == MOE_DT_E4M3 && w_dt == MOE_DT_E2M1) ? 1 : 0;
+  return moe_router_kernel_count(T, H, E, act_dt, gate_dt) + align + 3 + perm;
 }
 
 int moe_layer(const void* hidden, int act_dt, const uint8_t* hidden_scale, const void* gate,
@@ -639,7 +661,7 @@ int moe_layer(const void* hidden, int act_dt, const uint8_t* hidden_scale, const
                           align_ticket(ws)) != 0) {
     return launch_fail("align kernel");
   }
-  const FfnLayout FL = ffn_layout(T, F, E, k, block_m, true, ffn_dt);
+  const FfnLayout FL = ffn_layout(T, H, F, E, k, block_m, true, ffn_dt);
   void* inter = base + L.ffn + FL.inter;
   if (ffn_dt == MOE_DT_E4M3) {
     const void* xq = cast_input ? static_cast<const void*>(cq) : hidden;
@@ -647,8 +669,15 @@ int moe_layer(const void* hidden, int act_dt, const uint8_t* hidden_scale, const
     if (!xs || !w13_scale || !w2_scale) return MOE_ERR_ARG;
     uint8_t* iq = static_cast<uint8_t*>(inter);
     uint8_t* isc = iq + align_up(static_cast<size_t>(L.cap) * F, 256);
+    // an e4m3 hidden: its rows are permuted into the padded order in the
+    // workspace (room reserved by the layout), so GEMM1 reads them by TMA; a
+    // bf16 hidden's cast (whose workspace holds no permuted copy) is gathered
+    uint8_t* xp = cast_input ? nullptr : reinterpret_cast<uint8_t*>(base + L.ffn + FL.xperm);
+    uint8_t* xps =
+        cast_input ? nullptr : reinterpret_cast<uint8_t*>(base + L.ffn + FL.xperm_scale);
     rc = expert_gemm_lowbit(0, xq, xs, w13, w13_scale, T, H, F, E, k, block_m,
-                            sorted, blk, npp, L.cap, iq, isc, nullptr, nullptr, ws, s, naive);
+                            sorted, blk, npp, L.cap, iq, isc, nullptr, nullptr, ws, s, naive,
+                            xp, xps);
     if (rc != MOE_OK) return rc;
     rc = expert_gemm_lowbit(1, iq, isc, w2, w2_scale, T, H, F, E, k, block_m, sorted, blk, npp,
                             L.cap, nullptr, nullptr, wts, stage, ws, s, naive);

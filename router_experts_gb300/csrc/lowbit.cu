@@ -150,7 +150,11 @@ MOE_DEV int mx_wrow(const LowbitParams& p, const MxUnit& u, int r) {
   }
 }
 
-template <int KIND>
+// GATHER: GEMM1's token rows are gathered from x by sorted_ids (cp.async);
+// otherwise the A rows are already in the block's padded order (GEMM2's
+// intermediate, or GEMM1's rows permuted by permute_rows_kernel) and one 2-D
+// TMA copy per step loads them.
+template <int KIND, bool GATHER>
 __global__ void __launch_bounds__(kMxThreads, 1)
     lowbit_gemm_kernel(const __grid_constant__ CUtensorMap tm_w,
                        const __grid_constant__ CUtensorMap tm_wpf,
@@ -179,7 +183,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     for (int i = 0; i < kMxStages; ++i) {
       // weight TMA expect-tx arrival + tokens (GEMM1: 128 cp.async arrivals,
       // GEMM2: one TMA expect-tx arrival) + the four scale warps
-      mbar_init(&full[i], 1 + (KIND == 0 ? 128 : 1) + 4);
+      mbar_init(&full[i], 1 + (GATHER ? 128 : 1) + 4);
       mbar_init(&empty[i], 1);  // MMA commit
     }
     for (int i = 0; i < 2; ++i) {
@@ -268,7 +272,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
             alive = false;
             break;
           }
-          if constexpr (KIND == 0) fence_proxy_async_smem();  // cp.async rows -> tensor core
+          if constexpr (GATHER) fence_proxy_async_smem();  // cp.async rows -> tensor core
           tc_fence_after();
           const uint32_t a_addr = smem_u32(smem + s * kMxStageBytes);
           const uint32_t b_addr = a_addr + kMxTile;
@@ -286,7 +290,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     }
   } else if (warp < 6) {
     // ---------------- token tiles ----------------
-    if constexpr (KIND == 0) {
+    if constexpr (GATHER) {
       // cp.async gather: thread gt copies 16-byte chunk gt % 8 of tile rows
       // gt/8 + 16i; its arrival counts when its copies have landed (the MMA
       // thread fences before the tensor core reads them)
@@ -370,7 +374,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
         pf_unit = un;
         const MxUnit u = decode(static_cast<int>(blockIdx.x) + un * static_cast<int>(gridDim.x));
         pa = nullptr;
-        if constexpr (KIND == 0) {
+        if constexpr (GATHER) {
           const int t = token_of(u, r);
           if (t >= 0) pa = p.act_scale + static_cast<size_t>(t) * (K / 32);
         } else {
@@ -509,6 +513,33 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   }
 }
 
+// GEMM1's token rows in the blocks' padded order: position q below the
+// padded length holds row a / k of x (codes and scale bytes) for its
+// assignment a = sorted_ids[q], so GEMM1 loads its A tiles with one 2-D TMA
+// copy per step as GEMM2 does.  Padding positions are not written: their
+// products reach only padding rows of the accumulators, which no epilogue
+// stores.  One warp per position: H bytes of codes in 16-byte pieces, H/32
+// scale bytes in 4-byte words (H % 128 == 0).
+__global__ void __launch_bounds__(256) permute_rows_kernel(const LowbitParams p, uint8_t* xq,
+                                                           uint8_t* xs) {
+  const int lane = threadIdx.x & 31;
+  const long long warps = static_cast<long long>(gridDim.x) * 8;
+  const int npp = padded_rows(p, p.BM);
+  const int nk = p.T * p.k;
+  const int H16 = p.H / 16, H128 = p.H / 128;
+  for (long long q = blockIdx.x * 8ll + (threadIdx.x >> 5); q < npp; q += warps) {
+    const int a = row_assignment(p, static_cast<int>(q / p.BM), p.BM, static_cast<int>(q % p.BM));
+    if (a < 0 || a >= nk) continue;
+    const uint4* src = reinterpret_cast<const uint4*>(p.act + static_cast<size_t>(a / p.k) * p.H);
+    uint4* dst = reinterpret_cast<uint4*>(xq + static_cast<size_t>(q) * p.H);
+    for (int i = lane; i < H16; i += 32) dst[i] = __ldg(src + i);
+    const uint32_t* ss =
+        reinterpret_cast<const uint32_t*>(p.act_scale + static_cast<size_t>(a / p.k) * (p.H / 32));
+    uint32_t* sd = reinterpret_cast<uint32_t*>(xs + static_cast<size_t>(q) * (p.H / 32));
+    for (int i = lane; i < H128; i += 32) sd[i] = __ldg(ss + i);
+  }
+}
+
 // FP8 cast of the layer input ("How GPUs Fuse ..." §1.1: a small kernel turns
 // the layer input into FP8 codes and writes the scales; the scale rule of
 // §3.5): bf16 x [T, H] -> e4m3 codes [T, H] and one UE8M0 byte per 32 values
@@ -534,11 +565,14 @@ int launch_cast_e4m3(const void* x, int T, int H, uint8_t* codes, uint8_t* scale
   return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 
-int launch_lowbit_gemm(int kind, const LowbitParams& p, int num_sms, cudaStream_t stream) {
-  static std::atomic<unsigned long long> smem_set0{0}, smem_set1{0};
-  if (!ensure_smem_limit(reinterpret_cast<const void*>(lowbit_gemm_kernel<0>), kMxSmem,
+int launch_lowbit_gemm(int kind, const LowbitParams& p, int num_sms, cudaStream_t stream,
+                       uint8_t* xperm, uint8_t* xperm_scale) {
+  static std::atomic<unsigned long long> smem_set0{0}, smem_set0p{0}, smem_set1{0};
+  if (!ensure_smem_limit(reinterpret_cast<const void*>(lowbit_gemm_kernel<0, true>), kMxSmem,
                          smem_set0) ||
-      !ensure_smem_limit(reinterpret_cast<const void*>(lowbit_gemm_kernel<1>), kMxSmem,
+      !ensure_smem_limit(reinterpret_cast<const void*>(lowbit_gemm_kernel<0, false>), kMxSmem,
+                         smem_set0p) ||
+      !ensure_smem_limit(reinterpret_cast<const void*>(lowbit_gemm_kernel<1, false>), kMxSmem,
                          smem_set1))
     return -1;
   // packed weight codes [E*2F or E*H rows, K codes], box 128 codes x 64 rows;
@@ -549,16 +583,31 @@ int launch_lowbit_gemm(int kind, const LowbitParams& p, int num_sms, cudaStream_
   CUtensorMap tm_w, tm_wpf, tm_a;
   if (!make_map_e2m1(&tm_w, p.w, rows, static_cast<uint64_t>(K), 64)) return -1;
   if (!make_map_u8(&tm_wpf, p.w, rows, static_cast<uint64_t>(K) / 2, 64, 64)) return -1;
-  if (kind == 0) {
+  // token rows by TMA: one box = the data rows of a block
+  const uint32_t bmr = static_cast<uint32_t>(p.BM < 128 ? p.BM : 128);
+  if (kind == 0 && xperm == nullptr) {
     tm_a = tm_w;  // unused: GEMM1 gathers its token rows with cp.async
-    lowbit_gemm_kernel<0><<<num_sms, kMxThreads, kMxSmem, stream>>>(tm_w, tm_wpf, tm_a, p);
+    lowbit_gemm_kernel<0, true><<<num_sms, kMxThreads, kMxSmem, stream>>>(tm_w, tm_wpf, tm_a, p);
+  } else if (kind == 0) {
+    // GEMM1's rows permuted into the padded order first, then read like
+    // GEMM2 reads the intermediate
+    const long long warps_needed = (static_cast<long long>(p.cap_rows) + 7) / 8;
+    const int pblocks = static_cast<int>(warps_needed < num_sms * 8 ? warps_needed : num_sms * 8);
+    permute_rows_kernel<<<pblocks > 0 ? pblocks : 1, 256, 0, stream>>>(p, xperm, xperm_scale);
+    if (cudaGetLastError() != cudaSuccess) return -1;
+    if (!make_map_u8_sw128(&tm_a, xperm, static_cast<uint64_t>(p.cap_rows),
+                           static_cast<uint64_t>(p.H), bmr))
+      return -1;
+    LowbitParams q = p;
+    q.act = xperm;
+    q.act_scale = xperm_scale;
+    lowbit_gemm_kernel<0, false><<<num_sms, kMxThreads, kMxSmem, stream>>>(tm_w, tm_wpf, tm_a, q);
   } else {
-    // intermediate codes [cap_rows, F], one box = the data rows of a block
-    const uint32_t bmr = static_cast<uint32_t>(p.BM < 128 ? p.BM : 128);
+    // intermediate codes [cap_rows, F]
     if (!make_map_u8_sw128(&tm_a, p.act, static_cast<uint64_t>(p.cap_rows),
                            static_cast<uint64_t>(p.F), bmr))
       return -1;
-    lowbit_gemm_kernel<1><<<num_sms, kMxThreads, kMxSmem, stream>>>(tm_w, tm_wpf, tm_a, p);
+    lowbit_gemm_kernel<1, false><<<num_sms, kMxThreads, kMxSmem, stream>>>(tm_w, tm_wpf, tm_a, p);
   }
   return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }

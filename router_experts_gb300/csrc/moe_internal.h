@@ -149,7 +149,12 @@ struct LowbitParams {
   int cap_rows;
   int naive;                   // single-assignment blocks (see padded_rows)
 };
-int launch_lowbit_gemm(int kind, const LowbitParams& p, int num_sms, cudaStream_t stream);
+// xperm / xperm_scale (GEMM1 only; nullptr: gather the rows instead): room
+// for cap_rows x H codes and cap_rows x H/32 scale bytes, 256-byte aligned;
+// GEMM1 then launches a permutation of its token rows into the blocks'
+// padded order first and loads them by TMA.
+int launch_lowbit_gemm(int kind, const LowbitParams& p, int num_sms, cudaStream_t stream,
+                       uint8_t* xperm = nullptr, uint8_t* xperm_scale = nullptr);
 // bf16 x [T, H] (16-byte aligned, H % 32 == 0) -> e4m3 codes [T, H] (16-byte
 // aligned) and UE8M0 scale bytes [T, H/32].
 int launch_cast_e4m3(const void* x, int T, int H, uint8_t* codes, uint8_t* scales,

@@ -151,9 +151,10 @@ def test_layer_kernel_count(lib):
     assert lib.moe_layer_kernel_count(2, 2048, 768, 128, 8, 0, 0, 0) == 6
     assert lib.moe_layer_kernel_count(5, 2048, 768, 128, 8, 0, 0, 0) == 6
     assert lib.moe_layer_kernel_count(4096, 2048, 768, 128, 8, 0, 0, 0) == 6
-    assert lib.moe_layer_kernel_count(1, 4096, 2048, 256, 6, 2, 1, 3) == 4
-    assert lib.moe_layer_kernel_count(8, 4096, 2048, 256, 6, 2, 1, 3) == 7
-    assert lib.moe_layer_kernel_count(4096, 4096, 2048, 256, 6, 2, 1, 3) == 7
+    # (an e4m3 hidden with e2m1 experts: + the permutation of its rows)
+    assert lib.moe_layer_kernel_count(1, 4096, 2048, 256, 6, 2, 1, 3) == 5
+    assert lib.moe_layer_kernel_count(8, 4096, 2048, 256, 6, 2, 1, 3) == 8
+    assert lib.moe_layer_kernel_count(4096, 4096, 2048, 256, 6, 2, 1, 3) == 8
     assert lib.moe_layer_kernel_count(1, 2048, 768, 640, 8, 0, 0, 0) == 4
     assert lib.moe_layer_kernel_count(0, 2048, 768, 128, 8, 0, 0, 0) == 0
     # a bf16 hidden with e2m1 experts: the FP8 cast rides in the router's
