@@ -532,7 +532,16 @@ __global__ void __launch_bounds__(256) permute_rows_kernel(const LowbitParams p,
     if (a < 0 || a >= nk) continue;
     const uint4* src = reinterpret_cast<const uint4*>(p.act + static_cast<size_t>(a / p.k) * p.H);
     uint4* dst = reinterpret_cast<uint4*>(xq + static_cast<size_t>(q) * p.H);
-    for (int i = lane; i < H16; i += 32) dst[i] = __ldg(src + i);
+    // eight 16-byte loads in flight per lane before the stores
+    for (int i0 = lane; i0 < H16; i0 += 32 * 8) {
+      uint4 v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (i0 + 32 * u < H16) v[u] = __ldg(src + i0 + 32 * u);
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (i0 + 32 * u < H16) dst[i0 + 32 * u] = v[u];
+    }
     const uint32_t* ss =
         reinterpret_cast<const uint32_t*>(p.act_scale + static_cast<size_t>(a / p.k) * (p.H / 32));
     uint32_t* sd = reinterpret_cast<uint32_t*>(xs + static_cast<size_t>(q) * (p.H / 32));
