@@ -600,9 +600,11 @@ int launch_lowbit_gemm(int kind, const LowbitParams& p, int num_sms, cudaStream_
   } else if (kind == 0) {
     // GEMM1's rows permuted into the padded order first, then read like
     // GEMM2 reads the intermediate
-    const long long warps_needed = (static_cast<long long>(p.cap_rows) + 7) / 8;
-    const int pblocks = static_cast<int>(warps_needed < num_sms * 8 ? warps_needed : num_sms * 8);
-    permute_rows_kernel<<<pblocks > 0 ? pblocks : 1, 256, 0, stream>>>(p, xperm, xperm_scale);
+    // one warp per position of the capacity (eight per block), so every row
+    // copy is in flight at once
+    const long long pblocks = (static_cast<long long>(p.cap_rows) + 7) / 8;
+    permute_rows_kernel<<<static_cast<unsigned>(pblocks > 0 ? pblocks : 1), 256, 0, stream>>>(
+        p, xperm, xperm_scale);
     if (cudaGetLastError() != cudaSuccess) return -1;
     if (!make_map_u8_sw128(&tm_a, xperm, static_cast<uint64_t>(p.cap_rows),
                            static_cast<uint64_t>(p.H), bmr))
