@@ -16,7 +16,7 @@
 // and the one thread that issues the MMAs does little else per K step than
 // wait on one barrier, issue four MMAs and one commit (every tcgen05
 // instruction costs that thread tens of nanoseconds):
-//   B = 128 weight rows, loaded by TMA straight from the packed e2m1 codes
+//   B = 256 weight rows, loaded by TMA straight from the packed e2m1 codes
 //       with the 16 x 4-bit / 16-byte tensor-map type: each 16 codes land as
 //       their 8 packed bytes plus an 8-byte gap, the MMA's 4-bit operand
 //       layout (the copy counts the packed bytes in its transactions);
@@ -30,14 +30,19 @@
 //       column base + 4 + n/32; byte j scales K-block j of the step.  The
 //       words are staged in groups of 4 steps (one 16-byte copy per row and
 //       operand) a few groups ahead.
-// Tile: M = 128 token rows of one block (BLOCK_M rows valid), N = 128 weight
-// rows (GEMM1: 64 gate rows + the matching 64 up rows), K steps of 128 (four
-// K = 32 MMAs).  One ring of K steps (token tile + weight tile + an 8-column
-// TMEM scale slot) with one full and one empty barrier per step.  Two
-// 128-column accumulators, double-buffered.
+// Tile: M = 128 token rows of one block (BLOCK_M rows valid), N = 256 weight
+// rows (GEMM1: 128 gate rows + the matching 128 up rows), K steps of 128
+// (four K = 32 MMAs).  One ring of K steps (token tile + weight tile + a
+// 16-column TMEM scale slot) with one full and one empty barrier per step.
+// The 256-column accumulator and the scale slots fill the 512 TMEM columns
+// but for one accumulator, so the next tile's MMAs start once the epilogue
+// has read the accumulator (its loads run ahead meanwhile); against 128-row
+// weight tiles with two accumulators, each token tile feeds twice the MMA
+// work and the MMA thread issues half the instructions per FLOP, which is
+// what bounded the step (operand latency over the ring's depth, and about
+// 40 ns per MMA instruction).
 // 14 warps:
-//   warp 0      TMA of the weight tiles (L2 warmed kMxL2Ahead steps ahead
-//               through a plain byte map of the same codes)
+//   warp 0      TMA of the weight tiles
 //   warp 1      TMEM allocation and the single thread issuing the MMAs
 //   warps 2-5   token tiles (GEMM1 cp.async gather; GEMM2 one TMA copy)
 //   warps 6-9   scale words -> TMEM (lane quarter = warp % 4)
@@ -53,22 +58,25 @@ namespace {
 
 constexpr int kMxThreads = 448;
 constexpr int kMxBK = 128;                  // K values per stage (4 MMAs of K = 32)
-constexpr int kMxNT = 128;                  // weight rows per tile (MMA N)
-constexpr int kMxStages = 6;                // ring of K steps
-constexpr int kMxL2Ahead = 12;              // weight steps warmed in L2 ahead of their load
+constexpr int kMxNT = 256;                  // weight rows per tile (MMA N)
+constexpr int kMxStages = 4;                // ring of K steps
 constexpr int kMxSfSlots = 3;               // scale staging slots, 4 K steps each
-constexpr int kMxTile = 128 * kMxBK;        // 16 KB per operand tile (one byte per code in smem)
-constexpr int kMxStageBytes = 2 * kMxTile;  // token tile + weight tile
-// scale staging: [kMxSfSlots][token | weight][128 rows][4 steps x 4 bytes]
-constexpr int kMxSfStageBytes = kMxSfSlots * 2 * 128 * 16;
+constexpr int kMxATile = 128 * kMxBK;       // 16 KB token tile (one byte per code)
+constexpr int kMxBTile = kMxNT * kMxBK;     // 32 KB weight tile (one byte per 4-bit code in smem)
+constexpr int kMxStageBytes = kMxATile + kMxBTile;
+// scale staging: [kMxSfSlots][token rows 0..127 | weight rows 0..255][4 steps x 4 bytes]
+constexpr int kMxSfSlotBytes = (128 + kMxNT) * 16;
+constexpr int kMxSfStageBytes = kMxSfSlots * kMxSfSlotBytes;
 constexpr int kMxBarBytes = 256;
 constexpr int kMxSmem = kMxStages * kMxStageBytes + kMxSfStageBytes + kMxBarBytes + 1024;
 static_assert(kMxSmem <= 232448, "shared memory budget");
-constexpr uint32_t kMxAccCols = 128;        // per accumulator buffer
-constexpr uint32_t kMxSfCol0 = 256;         // scale slots: 8 columns per ring stage
+static_assert(kMxStageBytes % 1024 == 0, "stage tiles must keep 1024-byte alignment");
+constexpr uint32_t kMxAccCols = kMxNT;      // one accumulator
+constexpr uint32_t kMxSfCol0 = kMxAccCols;  // scale slots after it
+constexpr uint32_t kMxSfCols = 16;          // per ring stage: A at +0..3, B at +4..11
 constexpr uint32_t kMxTmemCols = 512;
-static_assert(kMxSfCol0 + 8 * kMxStages <= kMxTmemCols, "TMEM columns");
-static_assert(2 * (kMxStages + 2) * 8 + 8 <= kMxBarBytes, "barrier space");
+static_assert(kMxSfCol0 + kMxSfCols * kMxStages <= kMxTmemCols, "TMEM columns");
+static_assert(2 * (kMxStages + 1) * 8 + 8 <= kMxBarBytes, "barrier space");
 
 // Instruction descriptor of the block-scaled MMA: e4m3 A, e2m1 B (both
 // K-major), UE8M0 scales, fp32 D; sf_id picks the scale byte of the 32-bit
@@ -138,16 +146,25 @@ struct MxUnit {
   int b, n, e;
 };
 
-// Weight row r (0..127) of the tile of unit u: GEMM1 gate rows n*64 + r for
-// r < 64 and the matching up rows for r >= 64; GEMM2 rows n*128 + r.
+// Weight row r (0..255) of the tile of unit u: GEMM1 gate rows n*128 + r for
+// r < 128 and the matching up rows for r >= 128 (F % 128 == 0); GEMM2 rows
+// n*256 + r, held inside the expert's H rows: when H % 256 == 128 the last
+// tile's second half repeats rows of the expert, whose columns no epilogue
+// stores.
 template <int KIND>
 MOE_DEV int mx_wrow(const LowbitParams& p, const MxUnit& u, int r) {
   if constexpr (KIND == 0) {
-    const int f = u.n * (kMxNT / 2) + (r & 63);
-    return u.e * 2 * p.F + ((r < 64) ? 0 : p.F) + f;
+    const int f = u.n * (kMxNT / 2) + (r & 127);
+    return u.e * 2 * p.F + ((r < 128) ? 0 : p.F) + f;
   } else {
-    return u.e * p.H + u.n * kMxNT + r;
+    return u.e * p.H + min(u.n * kMxNT + r, p.H - 1);
   }
+}
+// First weight row of the 128-row box h (0, 1) of unit u's tile.
+template <int KIND>
+MOE_DEV int mx_wbox(const LowbitParams& p, const MxUnit& u, int h) {
+  if constexpr (KIND == 0) return u.e * 2 * p.F + h * p.F + u.n * (kMxNT / 2);
+  else return u.e * p.H + min(u.n * kMxNT + 128 * h, p.H - 128);
 }
 
 // GATHER: GEMM1's token rows are gathered from x by sorted_ids (cp.async);
@@ -157,25 +174,24 @@ MOE_DEV int mx_wrow(const LowbitParams& p, const MxUnit& u, int r) {
 template <int KIND, bool GATHER>
 __global__ void __launch_bounds__(kMxThreads, 1)
     lowbit_gemm_kernel(const __grid_constant__ CUtensorMap tm_w,
-                       const __grid_constant__ CUtensorMap tm_wpf,
                        const __grid_constant__ CUtensorMap tm_a, const LowbitParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  // ring stage s: token tile at s * kMxStageBytes, weight tile kMxTile after it
+  // ring stage s: token tile at s * kMxStageBytes, weight tile kMxATile after it
   uint32_t* sfstage = reinterpret_cast<uint32_t*>(smem + kMxStages * kMxStageBytes);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kMxStages * kMxStageBytes + kMxSfStageBytes);
   uint64_t* empty = full + kMxStages;
   uint64_t* tfull = empty + kMxStages;
-  uint64_t* tempty = tfull + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  uint64_t* tempty = tfull + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int K = (KIND == 0) ? p.H : p.F;
   const int KS = K / kMxBK;
   const int nblk = padded_rows(p, p.BM) / p.BM;
-  const int ntiles = (KIND == 0) ? p.F / (kMxNT / 2) : p.H / kMxNT;
+  const int ntiles = (KIND == 0) ? p.F / (kMxNT / 2) : (p.H + kMxNT - 1) / kMxNT;
   const int num_units = nblk * ntiles;
   const int bmr = min(p.BM, 128);  // token rows of a tile that hold data
 
@@ -186,10 +202,8 @@ __global__ void __launch_bounds__(kMxThreads, 1)
       mbar_init(&full[i], 1 + (GATHER ? 128 : 1) + 4);
       mbar_init(&empty[i], 1);  // MMA commit
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&tfull[i], 1);
-      mbar_init(&tempty[i], 4);
-    }
+    mbar_init(tfull, 1);
+    mbar_init(tempty, 4);
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -222,37 +236,22 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     // ---------------- weight tiles (TMA) ----------------
     if (lane == 0) {
       tma_prefetch_desc(&tm_w);
-      tma_prefetch_desc(&tm_wpf);
       uint32_t it = 0;
       bool alive = true;
       for (int uu = blockIdx.x; alive && uu < num_units; uu += gridDim.x) {
         const MxUnit u = decode(uu);
-        const int r0 = mx_wrow<KIND>(p, u, 0), r64 = mx_wrow<KIND>(p, u, 64);
-        // the next unit of this CTA, for warming L2 across the unit boundary
-        const bool has_next = uu + static_cast<int>(gridDim.x) < num_units;
-        const MxUnit nu = has_next ? decode(uu + gridDim.x) : u;
-        const int n0 = mx_wrow<KIND>(p, nu, 0), n64 = mx_wrow<KIND>(p, nu, 64);
+        const int r0 = mx_wbox<KIND>(p, u, 0), r1 = mx_wbox<KIND>(p, u, 1);
         for (int ks = 0; ks < KS; ++ks, ++it) {
-          int pk = ks + kMxL2Ahead, p0 = r0, p64 = r64;
-          if (pk >= KS && has_next) {
-            pk -= KS;
-            p0 = n0;
-            p64 = n64;
-          }
-          if (pk < KS) {  // byte map of the packed codes: x in bytes
-            tma_prefetch_l2_2d(&tm_wpf, pk * (kMxBK / 2), p0);
-            tma_prefetch_l2_2d(&tm_wpf, pk * (kMxBK / 2), p64);
-          }
           const int s = it % kMxStages;
           if (!mbar_wait(&empty[s], ((it / kMxStages) & 1u) ^ 1u, abort_flag, p.err)) {
             alive = false;
             break;
           }
-          uint8_t* dst = smem + s * kMxStageBytes + kMxTile;
-          // two 64-row boxes of 128 codes: 2 x 64 x 64 packed bytes
+          uint8_t* dst = smem + s * kMxStageBytes + kMxATile;
+          // two 128-row boxes of 128 codes: 2 x 128 x 64 packed bytes
           mbar_arrive_expect_tx(&full[s], kMxNT * kMxBK / 2);
           tma_load_2d(dst, &tm_w, &full[s], ks * kMxBK, r0);
-          tma_load_2d(dst + 64 * 128, &tm_w, &full[s], ks * kMxBK, r64);
+          tma_load_2d(dst + 128 * 128, &tm_w, &full[s], ks * kMxBK, r1);
         }
       }
     }
@@ -262,10 +261,9 @@ __global__ void __launch_bounds__(kMxThreads, 1)
       uint32_t it = 0, acc_it = 0;
       bool alive = true;
       for (int uu = blockIdx.x; alive && uu < num_units; uu += gridDim.x, ++acc_it) {
-        const int buf = acc_it & 1;
-        if (!mbar_wait(&tempty[buf], ((acc_it >> 1) & 1u) ^ 1u, abort_flag, p.err)) break;
+        if (!mbar_wait(tempty, (acc_it & 1u) ^ 1u, abort_flag, p.err)) break;
         tc_fence_after();
-        const uint32_t d = tmem_base + buf * kMxAccCols;
+        const uint32_t d = tmem_base;
         for (int ks = 0; ks < KS; ++ks, ++it) {
           const int s = it % kMxStages;
           if (!mbar_wait(&full[s], (it / kMxStages) & 1u, abort_flag, p.err)) {
@@ -275,8 +273,8 @@ __global__ void __launch_bounds__(kMxThreads, 1)
           if constexpr (GATHER) fence_proxy_async_smem();  // cp.async rows -> tensor core
           tc_fence_after();
           const uint32_t a_addr = smem_u32(smem + s * kMxStageBytes);
-          const uint32_t b_addr = a_addr + kMxTile;
-          const uint32_t sf_t = tmem_base + kMxSfCol0 + 8 * s;
+          const uint32_t b_addr = a_addr + kMxATile;
+          const uint32_t sf_t = tmem_base + kMxSfCol0 + kMxSfCols * s;
 #pragma unroll
           for (int kk = 0; kk < kMxBK / 32; ++kk)
             umma_mxf8f4(d, sw128_desc(a_addr + kk * 32), sw128_desc(b_addr + kk * 32),
@@ -285,7 +283,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
           umma_commit(&empty[s]);
         }
         if (!alive) break;
-        umma_commit(&tfull[buf]);
+        umma_commit(tfull);
       }
     }
   } else if (warp < 6) {
@@ -346,16 +344,16 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     // ---------------- scale words -> TMEM ----------------
     // The four warps (lane quarter q = warp % 4) stage the scale words of
     // groups of 4 K steps in a ring of kMxSfSlots slots; thread (q, l) copies
-    // those of token row 32q + l and of weight row 32q + l (16 bytes = 4 steps
-    // when a scale row is a multiple of 16 bytes, else one word per step),
-    // kMxSfSlots - 1 groups ahead.  After a named barrier of the four warps
-    // every thread reads the word of its token row and the words of weight
-    // rows l, 32 + l, 64 + l, 96 + l, and stores them into the step's TMEM
-    // slot once the MMAs that last read that slot are done.
+    // those of token row 32q + l and of weight rows 32q + l and 128 + 32q + l
+    // (16 bytes = 4 steps when a scale row is a multiple of 16 bytes, else
+    // one word per step), kMxSfSlots - 1 groups ahead.  After a named barrier
+    // of the four warps every thread reads the word of its token row and the
+    // words of weight rows 32c + l (c = 0..7), and stores them into the
+    // step's TMEM slot once the MMAs that last read that slot are done.
     const int q = warp & 3;
     const int r = 32 * q + lane;  // staged row of this thread
     const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-    const uint32_t stage_base = smem_u32(sfstage);  // [slot][A | B][128 rows][16 bytes]
+    const uint32_t stage_base = smem_u32(sfstage);  // [slot][A 128 | B 256 rows][16 bytes]
     const int my_units = num_units > static_cast<int>(blockIdx.x)
                              ? (num_units - static_cast<int>(blockIdx.x) + gridDim.x - 1) / gridDim.x
                              : 0;
@@ -368,6 +366,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     int pf_unit = -1;
     const uint8_t* pa = nullptr;
     const uint8_t* pb = nullptr;
+    const uint8_t* pb2 = nullptr;
     auto issue = [&](int g) {
       const int un = g / gpu, gi = g % gpu;
       if (un != pf_unit) {
@@ -381,17 +380,21 @@ __global__ void __launch_bounds__(kMxThreads, 1)
           if (r < p.BM) pa = p.act_scale + (static_cast<size_t>(u.b) * p.BM + r) * (K / 32);
         }
         pb = p.w_scale + static_cast<size_t>(mx_wrow<KIND>(p, u, r)) * (K / 32);
+        pb2 = p.w_scale + static_cast<size_t>(mx_wrow<KIND>(p, u, r + 128)) * (K / 32);
       }
-      const uint32_t dst = stage_base + (g % kMxSfSlots) * 4096 + r * 16;
+      const uint32_t dst = stage_base + (g % kMxSfSlots) * kMxSfSlotBytes + r * 16;
+      const uint32_t dstb = stage_base + (g % kMxSfSlots) * kMxSfSlotBytes + 2048 + r * 16;
       if (wide) {
         cp_async_16(dst, pa ? static_cast<const void*>(pa + 16 * gi) : p.act_scale, pa ? 16u : 0u);
-        cp_async_16(dst + 2048, pb + 16 * gi, 16u);
+        cp_async_16(dstb, pb + 16 * gi, 16u);
+        cp_async_16(dstb + 2048, pb2 + 16 * gi, 16u);
       } else {
         const int nw = min(4, KS - 4 * gi);
         for (int w = 0; w < nw; ++w) {
           cp_async_4(dst + 4 * w, pa ? static_cast<const void*>(pa + 16 * gi + 4 * w) : p.act_scale,
                      pa ? 4u : 0u);
-          cp_async_4(dst + 2048 + 4 * w, pb + 16 * gi + 4 * w, 4u);
+          cp_async_4(dstb + 4 * w, pb + 16 * gi + 4 * w, 4u);
+          cp_async_4(dstb + 2048 + 4 * w, pb2 + 16 * gi + 4 * w, 4u);
         }
       }
     };
@@ -407,15 +410,15 @@ __global__ void __launch_bounds__(kMxThreads, 1)
       named_bar_sync(2, 128);
       if (g + kMxSfSlots - 1 < n_g) issue(g + kMxSfSlots - 1);
       cp_async_commit();  // one group per iteration (empty past the end)
-      const uint32_t slot = stage_base + (g % kMxSfSlots) * 4096;
+      const uint32_t slot = stage_base + (g % kMxSfSlots) * kMxSfSlotBytes;
       const int gi = g % gpu;
       const int j0 = (g / gpu) * KS + 4 * gi;
       const int nst = min(4, KS - 4 * gi);
       for (int t = 0; t < nst; ++t) {
         const uint32_t wa = ld_shared_u32(slot + r * 16 + 4 * t);
-        uint32_t wb[4];
+        uint32_t wb[8];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) wb[c] = ld_shared_u32(slot + 2048 + (32 * c + lane) * 16 + 4 * t);
+        for (int c = 0; c < 8; ++c) wb[c] = ld_shared_u32(slot + 2048 + (32 * c + lane) * 16 + 4 * t);
         const int j = j0 + t;
         const int s = j % kMxStages;
         // the slot's previous scales were read by the MMAs of step j - kMxStages
@@ -424,9 +427,10 @@ __global__ void __launch_bounds__(kMxThreads, 1)
           alive = false;
           break;
         }
-        const uint32_t col = kMxSfCol0 + 8 * s;
+        const uint32_t col = kMxSfCol0 + kMxSfCols * s;
         tmem_st1(lane_base + col + q, wa);
         tmem_st4(lane_base + col + 4, wb[0], wb[1], wb[2], wb[3]);
+        tmem_st4(lane_base + col + 8, wb[4], wb[5], wb[6], wb[7]);
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
@@ -441,30 +445,37 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     const int ew = warp & 3;
     const int row = ew * 32 + lane;
     uint32_t acc_it = 0;
+    // the accumulator is handed back to the MMA thread as soon as the last
+    // columns are in registers
+    auto release = [&]() {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty);
+    };
     for (int uu = blockIdx.x; uu < num_units; uu += gridDim.x, ++acc_it) {
       const MxUnit u = decode(uu);
-      const int buf = acc_it & 1;
-      const uint32_t aph = (acc_it >> 1) & 1u;
-      const bool ok = mbar_wait(&tfull[buf], aph, abort_flag, p.err);
+      const bool ok = mbar_wait(tfull, acc_it & 1u, abort_flag, p.err);
       if (named_bar_any(1, 128, !ok || *abort_flag)) break;
       tc_fence_after();
-      const uint32_t tb = tmem_base + (static_cast<uint32_t>(ew * 32) << 16) + buf * kMxAccCols;
+      const uint32_t tb = tmem_base + (static_cast<uint32_t>(ew * 32) << 16);
       const bool rvalid = row < p.BM;
       const size_t prow = static_cast<size_t>(u.b) * p.BM + row;
       if constexpr (KIND == 0) {
-        // SwiGLU of gate column c and up column 64 + c, re-quantised per 32
+        // SwiGLU of gate column c and up column 128 + c, re-quantised per 32
+        constexpr int NJ = kMxNT / 64;
 #pragma unroll 1
-        for (int j = 0; j < 2; ++j) {
+        for (int j = 0; j < NJ; ++j) {
           uint32_t g0[16], g1[16], u0[16], u1[16];
           tmem_ld16(tb + 32 * j, g0);
           tmem_ld16(tb + 32 * j + 16, g1);
-          tmem_ld16(tb + 64 + 32 * j, u0);
-          tmem_ld16(tb + 64 + 32 * j + 16, u1);
+          tmem_ld16(tb + kMxNT / 2 + 32 * j, u0);
+          tmem_ld16(tb + kMxNT / 2 + 32 * j + 16, u1);
           tmem_ld_wait();
           reg_fence16(g0);
           reg_fence16(g1);
           reg_fence16(u0);
           reg_fence16(u1);
+          if (j == NJ - 1) release();
           float act[32];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
@@ -484,25 +495,33 @@ __global__ void __launch_bounds__(kMxThreads, 1)
         if (rvalid) a = row_assignment(p, u.b, p.BM, row);
         const bool valid = rvalid && a >= 0 && a < p.T * p.k;
         const float w = valid ? __ldg(p.topk_weights + a) : 0.f;
-#pragma unroll 1
-        for (int c = 0; c < kMxNT / 16; ++c) {
-          uint32_t r[16];
-          tmem_ld16(tb + 16 * c, r);
-          tmem_ld_wait();
-          reg_fence16(r);
+        // 16-column chunks, the TMEM load of chunk c + 1 in flight while
+        // chunk c is scaled and stored
+        constexpr int NCH = kMxNT / 16;
+        uint32_t r[2][16];
+        tmem_ld16(tb, r[0]);
+        tmem_ld_wait();
+        reg_fence16(r[0]);
+#pragma unroll
+        for (int c = 0; c < NCH; ++c) {
+          const int cur = c & 1, nxt = cur ^ 1;
+          if (c + 1 < NCH) tmem_ld16(tb + 16 * (c + 1), r[nxt]);
           const int h = u.n * kMxNT + 16 * c;
           if (valid && h + 16 <= p.H) {
             uint32_t o[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i)
-              o[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * w, __uint_as_float(r[2 * i + 1]) * w);
+              o[i] = pack_bf16x2(__uint_as_float(r[cur][2 * i]) * w,
+                                 __uint_as_float(r[cur][2 * i + 1]) * w);
             st_global_v8(p.stage + static_cast<size_t>(a) * p.H + h, o);
+          }
+          if (c + 1 < NCH) {
+            tmem_ld_wait();
+            reg_fence16(r[nxt]);
+            if (c + 1 == NCH - 1) release();
           }
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[buf]);
     }
   }
 
@@ -584,19 +603,17 @@ int launch_lowbit_gemm(int kind, const LowbitParams& p, int num_sms, cudaStream_
       !ensure_smem_limit(reinterpret_cast<const void*>(lowbit_gemm_kernel<1, false>), kMxSmem,
                          smem_set1))
     return -1;
-  // packed weight codes [E*2F or E*H rows, K codes], box 128 codes x 64 rows;
-  // the same bytes as a plain byte map (box 64 bytes x 64 rows) for the L2 warm-up
+  // packed weight codes [E*2F or E*H rows, K codes], box 128 codes x 128 rows
   const int K = (kind == 0) ? p.H : p.F;
   const uint64_t rows = (kind == 0) ? static_cast<uint64_t>(p.E) * 2 * p.F
                                     : static_cast<uint64_t>(p.E) * p.H;
-  CUtensorMap tm_w, tm_wpf, tm_a;
-  if (!make_map_e2m1(&tm_w, p.w, rows, static_cast<uint64_t>(K), 64)) return -1;
-  if (!make_map_u8(&tm_wpf, p.w, rows, static_cast<uint64_t>(K) / 2, 64, 64)) return -1;
+  CUtensorMap tm_w, tm_a;
+  if (!make_map_e2m1(&tm_w, p.w, rows, static_cast<uint64_t>(K), 128)) return -1;
   // token rows by TMA: one box = the data rows of a block
   const uint32_t bmr = static_cast<uint32_t>(p.BM < 128 ? p.BM : 128);
   if (kind == 0 && xperm == nullptr) {
     tm_a = tm_w;  // unused: GEMM1 gathers its token rows with cp.async
-    lowbit_gemm_kernel<0, true><<<num_sms, kMxThreads, kMxSmem, stream>>>(tm_w, tm_wpf, tm_a, p);
+    lowbit_gemm_kernel<0, true><<<num_sms, kMxThreads, kMxSmem, stream>>>(tm_w, tm_a, p);
   } else if (kind == 0) {
     // GEMM1's rows permuted into the padded order first, then read like
     // GEMM2 reads the intermediate
@@ -612,13 +629,13 @@ int launch_lowbit_gemm(int kind, const LowbitParams& p, int num_sms, cudaStream_
     LowbitParams q = p;
     q.act = xperm;
     q.act_scale = xperm_scale;
-    lowbit_gemm_kernel<0, false><<<num_sms, kMxThreads, kMxSmem, stream>>>(tm_w, tm_wpf, tm_a, q);
+    lowbit_gemm_kernel<0, false><<<num_sms, kMxThreads, kMxSmem, stream>>>(tm_w, tm_a, q);
   } else {
     // intermediate codes [cap_rows, F]
     if (!make_map_u8_sw128(&tm_a, p.act, static_cast<uint64_t>(p.cap_rows),
                            static_cast<uint64_t>(p.F), bmr))
       return -1;
-    lowbit_gemm_kernel<1, false><<<num_sms, kMxThreads, kMxSmem, stream>>>(tm_w, tm_wpf, tm_a, p);
+    lowbit_gemm_kernel<1, false><<<num_sms, kMxThreads, kMxSmem, stream>>>(tm_w, tm_a, p);
   }
   return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
