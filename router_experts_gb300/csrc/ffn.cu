@@ -553,10 +553,11 @@ struct PairCfg {
 };
 
 // The task list, identical in every CTA: paired tasks (blocks b, b+1 of one
-// expert) in block order, then the solo blocks two per task (the second slot
-// kNoBlock when their number is odd).  All threads; scratch: nblk ints of
-// shared memory the ring lends before its first load.
-template <int NTHREADS>
+// expert) in block order, then the solo blocks, two per task (SOLO_PAIRS;
+// the second slot kNoBlock when their number is odd) or one per task (the
+// second slot kNoBlock).  All threads; scratch: nblk ints of shared memory
+// the ring lends before its first load.
+template <int NTHREADS, bool SOLO_PAIRS = true>
 MOE_DEV int build_pair_tasks(const int32_t* block_expert, int nblk, uint16_t* tb0, uint16_t* tb1,
                              uint8_t* tpair, int* scratch) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -618,19 +619,26 @@ MOE_DEV int build_pair_tasks(const int32_t* block_expert, int nblk, uint16_t* tb
       before += 1;
     } else if ((L & 1) && j == L - 1) {
       const int is = before >> 16;
-      const int t = NP + is / 2;
-      if ((is & 1) == 0) {
-        tb0[t] = static_cast<uint16_t>(b);
-        if (is == NS - 1) tb1[t] = kNoBlock;
+      if constexpr (SOLO_PAIRS) {
+        const int t = NP + is / 2;
+        if ((is & 1) == 0) {
+          tb0[t] = static_cast<uint16_t>(b);
+          if (is == NS - 1) tb1[t] = kNoBlock;
+        } else {
+          tb1[t] = static_cast<uint16_t>(b);
+        }
+        tpair[t] = 0;
       } else {
-        tb1[t] = static_cast<uint16_t>(b);
+        const int t = NP + is;
+        tb0[t] = static_cast<uint16_t>(b);
+        tb1[t] = kNoBlock;
+        tpair[t] = 0;
       }
-      tpair[t] = 0;
       before += 1 << 16;
     }
   }
   __syncthreads();
-  return NP + (NS + 1) / 2;
+  return NP + (SOLO_PAIRS ? (NS + 1) / 2 : NS);
 }
 
 template <int KIND, int GW>
@@ -952,13 +960,15 @@ int launch_kind(const CUtensorMap& tw, const CUtensorMap& tin, const FfnParams& 
 
 template <int KIND, int GW>
 int launch_pair(const CUtensorMap& tw, const CUtensorMap& tin, const FfnParams& p, int num_sms,
-                cudaStream_t stream) {
+                cudaStream_t stream, const char** why) {
   using PC = PairCfg<KIND, GW>;
   using C = Cfg<KIND, 128, GW>;
   static std::atomic<unsigned long long> smem_set{0};
   if (!ensure_smem_limit(reinterpret_cast<const void*>(ffn_pair_kernel<KIND, GW>),
-                         PC::SMEM_BYTES, smem_set))
+                         PC::SMEM_BYTES, smem_set)) {
+    *why = "CTA-pair kernel: shared-memory limit not accepted";
     return -1;
+  }
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -974,11 +984,19 @@ int launch_pair(const CUtensorMap& tw, const CUtensorMap& tin, const FfnParams& 
   // as many CTA pairs as fit at once (a GPC with an odd number of free SMs
   // leaves one out): the kernel is persistent, every pair must be resident
   int nclusters = 0;
-  if (cudaOccupancyMaxActiveClusters(&nclusters, ffn_pair_kernel<KIND, GW>, &cfg) != cudaSuccess ||
-      nclusters < 1)
+  if (cudaOccupancyMaxActiveClusters(&nclusters, ffn_pair_kernel<KIND, GW>, &cfg) != cudaSuccess) {
+    *why = "CTA-pair kernel: cluster occupancy query failed";
     return -1;
+  }
+  if (nclusters < 1) {
+    *why = "CTA-pair kernel: no CTA pair fits on the device";
+    return -1;
+  }
   cfg.gridDim = dim3(2 * (nclusters < num_sms / 2 ? nclusters : num_sms / 2));
-  if (cudaLaunchKernelEx(&cfg, ffn_pair_kernel<KIND, GW>, tw, tin, p) != cudaSuccess) return -1;
+  if (cudaLaunchKernelEx(&cfg, ffn_pair_kernel<KIND, GW>, tw, tin, p) != cudaSuccess) {
+    *why = "CTA-pair kernel: launch failed";
+    return -1;
+  }
   return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 
@@ -1026,15 +1044,15 @@ int launch_ffn_gemm(int kind, int block_m, const void* w, const FfnParams& p, in
     if (block_m == 16) rc = launch_kind<0, 16>(tw, tin, p, num_sms, stream);
     else if (block_m == 64) rc = launch_kind<0, 64>(tw, tin, p, num_sms, stream);
     else if (p.H <= kGather4MaxH) rc = launch_kind<0, 128, 4>(tw, tin, p, num_sms, stream);
-    else if (pair) rc = launch_pair<0, 2>(tw, tin, p, num_sms, stream);
+    else if (pair) rc = launch_pair<0, 2>(tw, tin, p, num_sms, stream, why);
     else rc = launch_kind<0, 128>(tw, tin, p, num_sms, stream);
   } else {
     if (block_m == 16) rc = launch_kind<1, 16>(tw, tin, p, num_sms, stream);
     else if (block_m == 64) rc = launch_kind<1, 64>(tw, tin, p, num_sms, stream);
-    else if (pair) rc = launch_pair<1, 2>(tw, tin, p, num_sms, stream);
+    else if (pair) rc = launch_pair<1, 2>(tw, tin, p, num_sms, stream, why);
     else rc = launch_kind<1, 128>(tw, tin, p, num_sms, stream);
   }
-  if (rc != 0) *why = "kernel launch failed";
+  if (rc != 0 && **why == '\0') *why = "kernel launch failed";
   return rc;
 }
 

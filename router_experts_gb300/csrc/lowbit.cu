@@ -461,6 +461,11 @@ __global__ void __launch_bounds__(kMxThreads, 1)
       const bool rvalid = row < p.BM;
       const size_t prow = static_cast<size_t>(u.b) * p.BM + row;
       if constexpr (KIND == 0) {
+        // a padding row is written as zero codes with scale 2^0 (its token
+        // tile row may hold anything when the rows come permuted)
+        int a0 = p.T * p.k;
+        if (rvalid) a0 = row_assignment(p, u.b, p.BM, row);
+        const bool pad = a0 < 0 || a0 >= p.T * p.k;
         // SwiGLU of gate column c and up column 128 + c, re-quantised per 32
         constexpr int NJ = kMxNT / 64;
 #pragma unroll 1
@@ -483,7 +488,12 @@ __global__ void __launch_bounds__(kMxThreads, 1)
             act[16 + i] = swiglu_f(__uint_as_float(g1[i]), __uint_as_float(u1[i]));
           }
           uint32_t codes[8];
-          const uint32_t sbyte = requant32(act, codes);
+          uint32_t sbyte = requant32(act, codes);
+          if (pad) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) codes[i] = 0u;
+            sbyte = 127u;
+          }
           const int f = u.n * (kMxNT / 2) + 32 * j;
           if (rvalid && f + 32 <= p.F) {
             st_global_v8(p.inter_q + prow * p.F + f, codes);
@@ -536,8 +546,8 @@ __global__ void __launch_bounds__(kMxThreads, 1)
 // padded length holds row a / k of x (codes and scale bytes) for its
 // assignment a = sorted_ids[q], so GEMM1 loads its A tiles with one 2-D TMA
 // copy per step as GEMM2 does.  Padding positions are not written: their
-// products reach only padding rows of the accumulators, which no epilogue
-// stores.  One warp per position: H bytes of codes in 16-byte pieces, H/32
+// products reach only padding rows of the accumulators, for which the
+// epilogue writes zeros.  One warp per position: H bytes of codes in 16-byte pieces, H/32
 // scale bytes in 4-byte words (H % 128 == 0).
 __global__ void __launch_bounds__(256) permute_rows_kernel(const LowbitParams p, uint8_t* xq,
                                                            uint8_t* xs) {

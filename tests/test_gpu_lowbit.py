@@ -95,6 +95,45 @@ def test_lowbit_gemm_entry_points_compose():
     assert codes.dtype == torch.uint8 and isc.dtype == torch.uint8
 
 
+
+# GEMM1 reads its token rows permuted into the blocks' padded order when the
+# workspace has room for the copy, and gathers them from x otherwise: the
+# same tile contents and MMA order, so the same codes and scale bytes.  Pad
+# rows are zero codes with scale byte 127 (2^0) in both, also after an
+# earlier call left other token rows at those positions of the permuted copy.
+@pytest.mark.parametrize("T,BM", [(64, 16), (512, 64), (1024, 128)])
+def test_lowbit_gemm1_permuted_equals_gathered(T, BM):
+    w = W.WORKLOADS["v4lo"]
+    d = v4lo_inputs(T, seed=6)
+    lib = moe.load()
+    ws = moe.Workspace("cuda")
+    small = moe.Workspace("cuda")
+    for seed in (6, 8):
+        ids, _ = W.random_routing(T, w.k, w.E, seed=seed, skew=1.1)
+        s, b, npp = moe.align(ids.cuda(), w.E, BM)
+        cap = s.numel()
+        pq, ps = moe.expert_gemm1(d["hidden"], d["w13"], BM, s, b, npp, w.k, ws=ws,
+                                  x_scale=d["hidden_scale"], w13_scale=d["w13_scale"])
+        # a workspace of the header alone: the GEMM gathers the rows
+        hdr = lib.moe_align_workspace_bytes()
+        buf = small.get(hdr)
+        gq = torch.empty((cap, w.F), dtype=torch.uint8, device="cuda")
+        gs = torch.empty((cap, w.F // 32), dtype=torch.uint8, device="cuda")
+        rc = lib.moe_expert_gemm1(moe._p(d["hidden"]), moe.DT_E4M3, moe._p(d["hidden_scale"]),
+                                  moe._p(d["w13"]), moe._p(d["w13_scale"]), moe.DT_E2M1, T, w.H,
+                                  w.F, w.E, w.k, BM, moe._p(s), moe._p(b), moe._p(npp), cap,
+                                  moe._p(gq), moe._p(gs), moe._p(buf), hdr, moe._stream())
+        assert rc == 0
+        torch.cuda.synchronize()
+        n = int(npp.item())
+        pad = (s[:n] >= T * w.k)
+        print(f"v4lo T={T} BM={BM} routing {seed}: {n // BM} row blocks, "
+              f"{int(pad.sum())} pad rows")
+        assert torch.equal(pq[:n], gq[:n]) and torch.equal(ps[:n], gs[:n])
+        assert int(pad.sum()) > 0
+        assert (pq[:n][pad] == 0).all() and (ps[:n][pad] == 127).all()
+        assert moe.read_device_error(ws.buf) == 0
+
 # T = 1 runs with single-assignment blocks (no align launch).  The oracle
 # routes every token (fp32 router inputs: the dequantised hidden rows and the
 # fp32 gate); at T = 4096 at least 256 tokens covering every row block are
