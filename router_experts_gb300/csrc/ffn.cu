@@ -553,11 +553,10 @@ struct PairCfg {
 };
 
 // The task list, identical in every CTA: paired tasks (blocks b, b+1 of one
-// expert) in block order, then the solo blocks, two per task (SOLO_PAIRS;
-// the second slot kNoBlock when their number is odd) or one per task (the
-// second slot kNoBlock).  All threads; scratch: nblk ints of shared memory
-// the ring lends before its first load.
-template <int NTHREADS, bool SOLO_PAIRS = true>
+// expert) in block order, then the solo blocks two per task (the second slot
+// kNoBlock when their number is odd).  All threads; scratch: nblk ints of
+// shared memory the ring lends before its first load.
+template <int NTHREADS>
 MOE_DEV int build_pair_tasks(const int32_t* block_expert, int nblk, uint16_t* tb0, uint16_t* tb1,
                              uint8_t* tpair, int* scratch) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -619,26 +618,19 @@ MOE_DEV int build_pair_tasks(const int32_t* block_expert, int nblk, uint16_t* tb
       before += 1;
     } else if ((L & 1) && j == L - 1) {
       const int is = before >> 16;
-      if constexpr (SOLO_PAIRS) {
-        const int t = NP + is / 2;
-        if ((is & 1) == 0) {
-          tb0[t] = static_cast<uint16_t>(b);
-          if (is == NS - 1) tb1[t] = kNoBlock;
-        } else {
-          tb1[t] = static_cast<uint16_t>(b);
-        }
-        tpair[t] = 0;
-      } else {
-        const int t = NP + is;
+      const int t = NP + is / 2;
+      if ((is & 1) == 0) {
         tb0[t] = static_cast<uint16_t>(b);
-        tb1[t] = kNoBlock;
-        tpair[t] = 0;
+        if (is == NS - 1) tb1[t] = kNoBlock;
+      } else {
+        tb1[t] = static_cast<uint16_t>(b);
       }
+      tpair[t] = 0;
       before += 1 << 16;
     }
   }
   __syncthreads();
-  return NP + (SOLO_PAIRS ? (NS + 1) / 2 : NS);
+  return NP + (NS + 1) / 2;
 }
 
 template <int KIND, int GW>
@@ -668,7 +660,8 @@ __global__ void __launch_bounds__(Cfg<KIND, 128, GW>::THREADS, 1)
                                                   reinterpret_cast<int*>(smem));
   fence_proxy_async_smem();  // the ring lent scratch: TMA writes it next
   const int ntiles = (KIND == 0) ? (p.F + 127) / 128 : (p.H + 255) / 256;
-  const int KB = ((KIND == 0) ? p.H : p.F) / kBK;
+  // K steps (GEMM2: F % 64 may be 32; the copy zero-fills past F)
+  const int KB = (((KIND == 0) ? p.H : p.F) + kBK - 1) / kBK;
   const int num_units = ntasks * ntiles;
 
   if (threadIdx.x == 0) {
@@ -983,14 +976,14 @@ int launch_pair(const CUtensorMap& tw, const CUtensorMap& tin, const FfnParams& 
   cfg.numAttrs = 1;
   // as many CTA pairs as fit at once (a GPC with an odd number of free SMs
   // leaves one out): the kernel is persistent, every pair must be resident
+  // (co-residency is for speed only: no CTA waits on another cluster, so
+  // when the query gives nothing, one pair per two SMs is launched and a
+  // pair that cannot be placed at once runs when one leaves)
   int nclusters = 0;
-  if (cudaOccupancyMaxActiveClusters(&nclusters, ffn_pair_kernel<KIND, GW>, &cfg) != cudaSuccess) {
-    *why = "CTA-pair kernel: cluster occupancy query failed";
-    return -1;
-  }
-  if (nclusters < 1) {
-    *why = "CTA-pair kernel: no CTA pair fits on the device";
-    return -1;
+  if (cudaOccupancyMaxActiveClusters(&nclusters, ffn_pair_kernel<KIND, GW>, &cfg) != cudaSuccess ||
+      nclusters < 1) {
+    (void)cudaGetLastError();
+    nclusters = num_sms / 2;
   }
   cfg.gridDim = dim3(2 * (nclusters < num_sms / 2 ? nclusters : num_sms / 2));
   if (cudaLaunchKernelEx(&cfg, ffn_pair_kernel<KIND, GW>, tw, tin, p) != cudaSuccess) {

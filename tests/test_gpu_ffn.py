@@ -21,7 +21,8 @@ def ffn_case(name, T, BM, skew=0.0, ntok=64, seed=1, ids=None, cover=False):
     """ntok >= T compares every token; cover=True picks at least ntok tokens
     so that every row block of the align output holds one of their
     assignments."""
-    w = W.WORKLOADS[name]
+    w = W.WORKLOADS[name] if isinstance(name, str) else name
+    name = w.name
     d = W.make_inputs(w, T, seed=seed, device="cuda")
     if ids is None:
         ids, wts = W.random_routing(T, w.k, w.E, seed=seed, skew=skew)
@@ -80,6 +81,16 @@ def test_ffn_all_tokens_one_expert(BM):
     ids = torch.full((T, 2), 0, dtype=torch.int32)
     ids[:, 1] = 5
     ffn_case("toy", T, BM, ids=ids, ntok=40)
+
+
+# 128-row tiles at sizes off the tile grid: F % 64 == 32 (GEMM2 ends on a
+# half K step, zero-filled by the copy), F below one 128-column tile, H below
+# and above 4096 (four and two gather warps), every expert with a pair of
+# blocks and an odd last block
+@pytest.mark.parametrize("H,F", [(128, 96), (4160, 96), (4160, 160)])
+def test_ffn_row_tiles_off_grid(H, F):
+    w = W.Workload("offgrid", H=H, E=4, k=2, F=F, scoring="softmax")
+    ffn_case(w, 600, 128, ntok=600)
 
 
 @pytest.mark.parametrize("BM", [16, 64])
