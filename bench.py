@@ -600,9 +600,12 @@ class LayerBench:
 def kernel_name(w, stage, BM, H):
     gw1 = 4 if (BM == 128 and H <= 4096) else 2
     if stage in ("gemm1", "gemm2"):
+        kind = 0 if stage == "gemm1" else 1
         if w.lowbit:
-            return "lowbit_gemm_kernel<%d>" % (0 if stage == "gemm1" else 1)
-        return "ffn_gemm_kernel<%d,%d,%d>" % ((0, BM, gw1) if stage == "gemm1" else (1, BM, 2))
+            return "lowbit_gemm_kernel<%d>" % kind
+        if BM == 128 and H > 4096:  # 128-row tiles on CTA pairs above H = 4096
+            return "ffn_pair_kernel<%d,2>" % kind
+        return "ffn_gemm_kernel<%d,%d,%d>" % ((0, BM, gw1) if kind == 0 else (1, BM, 2))
     return {"router": "router_gemm_kernel + router_select_kernel", "align": "align_kernel",
             "finalize": "finalize_kernel"}[stage]
 

@@ -108,13 +108,15 @@ typedef enum { MOE_DT_BF16 = 0, MOE_DT_F32 = 1, MOE_DT_E4M3 = 2, MOE_DT_E2M1 = 3
  * Execution.  When H % 64 == 0, E % 16 == 0 with E <= 256 (or E % 32 == 0
  * with E <= 512), hidden is BF16 or E4M3 and the gate is BF16 (or F32 with at
  * least 8 tokens): the gate GEMM runs on the tensor cores in 128-token tiles
- * with the K range split over CTAs, and a second launch sums each token's
- * split partials in split order and selects (plus one conversion launch
- * first when hidden is E4M3 or the gate is F32).  Otherwise ([P1] §5.1's
- * one-kernel router): one fused launch whose CTAs split the gate read and
- * whose last CTA per token tile selects.  On GB300 the two-launch path was
- * measured faster from the first token.  Both paths give the same ids except
- * where two rank keys are within fp32 summation-order noise of each other.
+ * with the K range split over CTAs; up to 4 tokens the CTA that finishes its
+ * token tile's splits last sums each token's partials in split order and
+ * selects (one launch), above that a second launch does (plus one conversion
+ * launch first when hidden is E4M3 or the gate is F32).  Otherwise ([P1]
+ * §5.1's one-kernel router): one fused launch whose CTAs split the gate read
+ * with mma.sync and whose last CTA per token tile selects.  On GB300 the
+ * tensor-core path was measured faster from the first token.  Both paths
+ * give the same ids except where two rank keys are within fp32
+ * summation-order noise of each other.
  * moe_router_kernel_count returns how many kernels moe_router enqueues for
  * these shapes and types (0 when T == 0).
  * ------------------------------------------------------------------------- */

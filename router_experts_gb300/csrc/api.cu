@@ -255,7 +255,7 @@ int moe_router_kernel_count(int T, int H, int E, int hidden_dt, int gate_dt) {
   if (T <= 0 || H <= 0 || E <= 0) return 0;
   const RouterPlan p = plan_router(T, H, E);
   if (!router_uses_tiled(p, hidden_dt, gate_dt)) return 1;
-  return 2 + ((hidden_dt == MOE_DT_E4M3 || gate_dt == MOE_DT_F32) ? 1 : 0);
+  return (p.fused_select ? 1 : 2) + ((hidden_dt == MOE_DT_E4M3 || gate_dt == MOE_DT_F32) ? 1 : 0);
 }
 
 int moe_router(const void* hidden, int hidden_dt, const uint8_t* hidden_scale, const void* gate,

@@ -61,9 +61,16 @@ struct RouterPlan {
   bool tiled;
   int tnt;        // token tiles of 128
   int tks;        // K splits across CTAs
+  bool fused_select;  // T <= kRouterFusedSelectMaxT: the GEMM's last CTA selects
   size_t xb_off, gp_off;  // offsets in the scratch of the bf16 x and the gate planes
   size_t scratch_bytes;
 };
+// Up to this many tokens the tensor-core router selects in the last CTA of
+// its gate GEMM (one launch; its six warps select one token each); above it
+// a selection kernel follows (measured on GB300: one launch saves 2 µs at
+// T = 1 for Qwen3, none for DeepSeek-V3, and costs 2-6 µs at T = 8, where
+// the last CTA's warps select twice in turn).
+constexpr int kRouterFusedSelectMaxT = 4;
 // allow_tiled = false keeps every T on the fused kernel.
 RouterPlan plan_router(int T, int H, int E, bool allow_tiled = true);
 // Argument rules shared by every router entry point: MOE_OK, MOE_ERR_ARG or

@@ -76,16 +76,57 @@ struct RgParams {
   uint32_t idesc;
 };
 
+// Every token's split partials summed in split order into the warp's row
+// buffer, then the selection; one warp per token.
+template <int S>
+MOE_DEV void select_from_partials(const RouterArgs& a, const float* part, int t, float* row,
+                                  const float* sbias) {
+  const int lane = threadIdx.x & 31;
+  const size_t slice = static_cast<size_t>(a.T) * a.E;
+  const float* src = part + static_cast<size_t>(t) * a.E;
+  float acc[S];
+#pragma unroll
+  for (int i = 0; i < S; ++i) acc[i] = 0.f;
+  // every load of a group of four splits is issued before any of them is summed
+  for (int s0 = 0; s0 < a.KS; s0 += 4) {
+    float v[4][S];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+      for (int i = 0; i < S; ++i) {
+        const int e = lane + 32 * i;
+        v[u][i] = (s0 + u < a.KS && e < a.E) ? __ldcg(src + (s0 + u) * slice + e) : 0.f;
+      }
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+      for (int i = 0; i < S; ++i) acc[i] += v[u][i];
+  }
+#pragma unroll
+  for (int i = 0; i < S; ++i)
+    if (lane + 32 * i < a.E) row[lane + 32 * i] = acc[i];
+  __syncwarp();
+  select_token<S>(a, t, row, sbias);
+  cast_token_row(a, t);
+}
+
+// S > 0 (few tokens): the CTA that finishes a token tile's K splits last
+// (acquire-release ticket per token tile, no spinning) also sums the
+// partials and selects the tile's tokens, one warp per token, so the router
+// is one launch; S = ceil(E / 32).  S = 0: partials only (the selection is
+// its own launch).
+template <int S>
 __global__ void __launch_bounds__(kRgThreads, 1)
     router_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
-                       const __grid_constant__ CUtensorMap tm_g, const RgParams p) {
+                       const __grid_constant__ CUtensorMap tm_g, const RgParams p,
+                       const RouterArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  const int S = p.stages;
-  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + S * p.stage_bytes);
-  uint64_t* empty_bar = full_bar + S;
-  uint64_t* acc_bar = empty_bar + S;
+  const int NS = p.stages;  // ring stages
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + NS * p.stage_bytes);
+  uint64_t* empty_bar = full_bar + NS;
+  uint64_t* acc_bar = empty_bar + NS;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -97,7 +138,7 @@ __global__ void __launch_bounds__(kRgThreads, 1)
   const uint32_t tcols = p.E <= 256 ? 256u : 512u;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < S; ++i) {
+    for (int i = 0; i < NS; ++i) {
       mbar_init(&full_bar[i], 1);
       mbar_init(&empty_bar[i], 1);
     }
@@ -117,8 +158,8 @@ __global__ void __launch_bounds__(kRgThreads, 1)
       tma_prefetch_desc(&tm_x);
       tma_prefetch_desc(&tm_g);
       for (int it = 0; it < nit; ++it) {
-        const int st = it % S;
-        const uint32_t ph = (it / S) & 1u;
+        const int st = it % NS;
+        const uint32_t ph = (it / NS) & 1u;
         if (!mbar_wait(&empty_bar[st], ph ^ 1u, abort_flag, p.err)) break;
         const int kb = kb0 + it / p.planes, pl = it % p.planes;
         uint8_t* sa = smem + st * p.stage_bytes;
@@ -134,8 +175,8 @@ __global__ void __launch_bounds__(kRgThreads, 1)
     if (lane == 0) {
       bool alive = true;
       for (int it = 0; it < nit; ++it) {
-        const int st = it % S;
-        const uint32_t ph = (it / S) & 1u;
+        const int st = it % NS;
+        const uint32_t ph = (it / NS) & 1u;
         if (!mbar_wait(&full_bar[st], ph, abort_flag, p.err)) {
           alive = false;
           break;
@@ -186,6 +227,28 @@ __global__ void __launch_bounds__(kRgThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem_base, tcols);
   }
+  if constexpr (S > 0) {
+    // one thread draws the ticket: release of this CTA's partials (stored
+    // before the barrier above), acquire of the other splits'
+    __shared__ int s_last;
+    if (threadIdx.x == 0) {
+      const int old = ticket_add_acq_rel(a.tickets + blockIdx.x, 1);
+      const int last = old == p.KS - 1;
+      if (last) store_relaxed_gpu(a.tickets + blockIdx.x, 0);  // ready for the next launch
+      s_last = last;
+    }
+    __syncthreads();
+    if (!s_last || *abort_flag) return;
+    // the ring is idle now (every stage was consumed before the accumulator
+    // was complete): it holds the bias and one row buffer per warp
+    float* sbias = reinterpret_cast<float*>(smem);
+    float* rows = sbias + 32 * S;
+    for (int e = threadIdx.x; e < a.E; e += kRgThreads) sbias[e] = a.bias ? __ldg(a.bias + e) : 0.f;
+    __syncthreads();
+    const int t_end = min(p.T, t0 + 128);
+    for (int t = t0 + warp; t < t_end; t += kRgThreads / 32)
+      select_from_partials<S>(a, p.part, t, rows + warp * 32 * S, sbias);
+  }
 }
 
 // Sum of each token's split partials (split order) and the selection; one
@@ -196,39 +259,13 @@ __global__ void __launch_bounds__(kRouterThreads) router_select_kernel(const Rou
                                                                        const float* part) {
   __shared__ __align__(16) float rows[8][32 * S];
   __shared__ float sbias[32 * S];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
   for (int e = threadIdx.x; e < a.E; e += kRouterThreads)
     sbias[e] = a.bias ? __ldg(a.bias + e) : 0.f;
   __syncthreads();
   const int t = blockIdx.x * 8 + warp;
   if (t >= a.T) return;
-  float* row = rows[warp];
-  const size_t slice = static_cast<size_t>(a.T) * a.E;
-  const float* src = part + static_cast<size_t>(t) * a.E;
-  float acc[S];
-#pragma unroll
-  for (int i = 0; i < S; ++i) acc[i] = 0.f;
-  // every load of a group of four splits is issued before any of them is summed
-  for (int s0 = 0; s0 < a.KS; s0 += 4) {
-    float v[4][S];
-#pragma unroll
-    for (int u = 0; u < 4; ++u)
-#pragma unroll
-      for (int i = 0; i < S; ++i) {
-        const int e = lane + 32 * i;
-        v[u][i] = (s0 + u < a.KS && e < a.E) ? __ldcg(src + (s0 + u) * slice + e) : 0.f;
-      }
-#pragma unroll
-    for (int u = 0; u < 4; ++u)
-#pragma unroll
-      for (int i = 0; i < S; ++i) acc[i] += v[u][i];
-  }
-#pragma unroll
-  for (int i = 0; i < S; ++i)
-    if (lane + 32 * i < a.E) row[lane + 32 * i] = acc[i];
-  __syncwarp();
-  select_token<S>(a, t, row, sbias);
-  cast_token_row(a, t);
+  select_from_partials<S>(a, part, t, rows[warp], sbias);
 }
 
 // Exact bf16 operands for the tiled gate GEMM: x e4m3 codes times their
@@ -283,6 +320,17 @@ int launch_typed(const RouterArgs& a, const RouterPlan& plan, cudaStream_t strea
   return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 
+template <int S>
+int launch_gemm(dim3 grid, int smem, cudaStream_t stream, const CUtensorMap& tm_x,
+                const CUtensorMap& tm_g, const RgParams& p, const RouterArgs& a) {
+  static std::atomic<unsigned long long> smem_set{0};
+  if (!ensure_smem_limit(reinterpret_cast<const void*>(router_gemm_kernel<S>),
+                         kRgSmemBudget + 1024 + kRgBarBytes, smem_set))
+    return -1;
+  router_gemm_kernel<S><<<grid, kRgThreads, smem, stream>>>(tm_x, tm_g, p, a);
+  return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
+
 int launch_tiled(RouterArgs a, int hidden_dt, int gate_dt, const RouterPlan& plan,
                  cudaStream_t stream) {
   const int T = a.T, H = a.H, E = a.E;
@@ -319,14 +367,19 @@ int launch_tiled(RouterArgs a, int hidden_dt, int gate_dt, const RouterPlan& pla
                      static_cast<uint64_t>(p.planes) * E, H, p.nb))
     return -1;
   const int smem = p.stages * p.stage_bytes + 1024 + kRgBarBytes;
-  static std::atomic<unsigned long long> smem_set{0};
-  if (!ensure_smem_limit(reinterpret_cast<const void*>(router_gemm_kernel),
-                         kRgSmemBudget + 1024 + kRgBarBytes, smem_set))
-    return -1;
-  router_gemm_kernel<<<dim3(plan.tnt, plan.tks), kRgThreads, smem, stream>>>(tm_x, tm_g, p);
-  if (cudaGetLastError() != cudaSuccess) return -1;
   a.KS = plan.tks;
   const int sl = (E + 31) / 32, blocks = (T + 7) / 8;
+  const dim3 grid(plan.tnt, plan.tks);
+  if (plan.fused_select) {
+    // the last CTA of the token tile selects: one launch
+    if (sl <= 1) return launch_gemm<1>(grid, smem, stream, tm_x, tm_g, p, a);
+    if (sl <= 2) return launch_gemm<2>(grid, smem, stream, tm_x, tm_g, p, a);
+    if (sl <= 4) return launch_gemm<4>(grid, smem, stream, tm_x, tm_g, p, a);
+    if (sl <= 8) return launch_gemm<8>(grid, smem, stream, tm_x, tm_g, p, a);
+    if (sl <= 9) return launch_gemm<9>(grid, smem, stream, tm_x, tm_g, p, a);
+    return launch_gemm<16>(grid, smem, stream, tm_x, tm_g, p, a);
+  }
+  if (launch_gemm<0>(grid, smem, stream, tm_x, tm_g, p, a) != 0) return -1;
   if (sl <= 1) router_select_kernel<1><<<blocks, kRouterThreads, 0, stream>>>(a, part);
   else if (sl <= 2) router_select_kernel<2><<<blocks, kRouterThreads, 0, stream>>>(a, part);
   else if (sl <= 4) router_select_kernel<4><<<blocks, kRouterThreads, 0, stream>>>(a, part);
@@ -364,6 +417,7 @@ RouterPlan plan_router(int T, int H, int E, bool allow_tiled) {
     p.gp_off = p.xb_off + align_up(static_cast<size_t>(T) * H * 2, 256);
     const size_t total = p.gp_off + align_up(static_cast<size_t>(3) * E * H * 2, 256);
     if (total > p.scratch_bytes) p.scratch_bytes = total;
+    p.fused_select = T <= kRouterFusedSelectMaxT;
   }
   return p;
 }

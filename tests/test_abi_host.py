@@ -143,14 +143,18 @@ def test_layer_and_cast_reject_bad_arguments(lib):
 
 
 def test_layer_kernel_count(lib):
-    # router launches (two for bf16 hidden and gate; one below 8 tokens for an
-    # fp32 gate; conversion + GEMM + selection for e4m3 hidden with an fp32
+    # router launches (bf16 hidden and gate: the gate GEMM, whose last CTA
+    # selects up to 4 tokens, then a selection kernel above that; one below 8
+    # tokens for an fp32 gate; + a conversion for e4m3 hidden with an fp32
     # gate; one for more experts than the tensor-core router covers), align
     # except for one token (single-assignment blocks), GEMM1, GEMM2, finalize
-    assert lib.moe_layer_kernel_count(1, 2048, 768, 128, 8, 0, 0, 0) == 5
-    assert lib.moe_layer_kernel_count(2, 2048, 768, 128, 8, 0, 0, 0) == 6
+    assert lib.moe_layer_kernel_count(1, 2048, 768, 128, 8, 0, 0, 0) == 4
+    assert lib.moe_layer_kernel_count(2, 2048, 768, 128, 8, 0, 0, 0) == 5
+    assert lib.moe_layer_kernel_count(4, 2048, 768, 128, 8, 0, 0, 0) == 5
     assert lib.moe_layer_kernel_count(5, 2048, 768, 128, 8, 0, 0, 0) == 6
     assert lib.moe_layer_kernel_count(4096, 2048, 768, 128, 8, 0, 0, 0) == 6
+    assert lib.moe_router_kernel_count(4, 2048, 128, 0, 0) == 1
+    assert lib.moe_router_kernel_count(5, 2048, 128, 0, 0) == 2
     # (an e4m3 hidden with e2m1 experts: + the permutation of its rows)
     assert lib.moe_layer_kernel_count(1, 4096, 2048, 256, 6, 2, 1, 3) == 5
     assert lib.moe_layer_kernel_count(8, 4096, 2048, 256, 6, 2, 1, 3) == 8

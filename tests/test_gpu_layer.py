@@ -162,7 +162,11 @@ def test_layer_equals_separate_calls(name, T):
     y2 = moe.finalize(st, T, w.k)
     torch.cuda.synchronize()
     print(f"layer {name} T={T}: equal to the separate calls")
-    assert moe.layer_kernel_count(T, w.H, w.F, w.E, w.k) == (5 if T == 1 else 6)
+    # router (one launch up to 4 tokens), align (none at one token), GEMM1,
+    # GEMM2, finalize
+    router = 1 if T <= 4 else 2
+    assert moe.router_kernel_count(T, w.H, w.E) == router
+    assert moe.layer_kernel_count(T, w.H, w.F, w.E, w.k) == router + (0 if T == 1 else 1) + 3
     assert torch.equal(y, y2)
     assert moe.read_device_error(moe.default_workspace("cuda").buf) == 0
 
