@@ -61,6 +61,7 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(const RouterArgs
 // to the fp32 value, each plane multiplied and accumulated in turn.
 // ---------------------------------------------------------------------------
 constexpr int kRgThreads = 192;  // warp 0 TMA, warp 1 MMA + TMEM, warps 2-5 epilogue
+constexpr int kRouterMaxSplits = 32;  // K splits of the tensor-core router (plan_router)
 constexpr int kRgBK = 64;        // K elements per stage (128 bytes of bf16)
 constexpr int kRgSmemBudget = 200 * 1024;
 constexpr int kRgBarBytes = 256;
@@ -240,14 +241,31 @@ __global__ void __launch_bounds__(kRgThreads, 1)
     __syncthreads();
     if (!s_last || *abort_flag) return;
     // the ring is idle now (every stage was consumed before the accumulator
-    // was complete): it holds the bias and one row buffer per warp
+    // was complete): it holds the bias and the tile's summed logits
     float* sbias = reinterpret_cast<float*>(smem);
-    float* rows = sbias + 32 * S;
+    float* rows = sbias + 32 * S;  // [tokens of the tile][E]
     for (int e = threadIdx.x; e < a.E; e += kRgThreads) sbias[e] = a.bias ? __ldg(a.bias + e) : 0.f;
-    __syncthreads();
     const int t_end = min(p.T, t0 + 128);
-    for (int t = t0 + warp; t < t_end; t += kRgThreads / 32)
-      select_from_partials<S>(a, p.part, t, rows + warp * 32 * S, sbias);
+    const int nt = t_end - t0;
+    // every thread sums (token, expert) pairs over the splits in split
+    // order, all of a pair's split loads in flight at once
+    const size_t slice = static_cast<size_t>(p.T) * a.E;
+    for (int pr = threadIdx.x; pr < nt * a.E; pr += kRgThreads) {
+      const int tt = pr / a.E, e = pr - tt * a.E;
+      const float* src = p.part + static_cast<size_t>(t0 + tt) * a.E + e;
+      float v[kRouterMaxSplits];
+#pragma unroll
+      for (int z2 = 0; z2 < kRouterMaxSplits; ++z2) v[z2] = z2 < p.KS ? __ldcg(src + z2 * slice) : 0.f;
+      float acc = 0.f;
+#pragma unroll
+      for (int z2 = 0; z2 < kRouterMaxSplits; ++z2) acc += v[z2];
+      rows[tt * a.E + e] = acc;
+    }
+    __syncthreads();
+    for (int t = t0 + warp; t < t_end; t += kRgThreads / 32) {
+      select_token<S>(a, t, rows + (t - t0) * a.E, sbias);
+      cast_token_row(a, t);
+    }
   }
 }
 
@@ -418,6 +436,19 @@ RouterPlan plan_router(int T, int H, int E, bool allow_tiled) {
     const size_t total = p.gp_off + align_up(static_cast<size_t>(3) * E * H * 2, 256);
     if (total > p.scratch_bytes) p.scratch_bytes = total;
     p.fused_select = T <= kRouterFusedSelectMaxT;
+    if (p.fused_select) {
+      // a few tokens: the gate read is the whole cost, so split K further
+      // (up to 32 CTAs, at least two K steps each) until each CTA's share is
+      // in flight at once
+      while (p.tks < 32 && KB / (2 * p.tks) >= 2) p.tks *= 2;
+      const size_t part2 = align_up(static_cast<size_t>(p.tks) * T * E * sizeof(float), 256);
+      if (part2 > p.xb_off) {
+        p.xb_off = part2;
+        p.gp_off = p.xb_off + align_up(static_cast<size_t>(T) * H * 2, 256);
+        const size_t total2 = p.gp_off + align_up(static_cast<size_t>(3) * E * H * 2, 256);
+        if (total2 > p.scratch_bytes) p.scratch_bytes = total2;
+      }
+    }
   }
   return p;
 }
