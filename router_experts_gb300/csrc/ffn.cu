@@ -904,20 +904,6 @@ bool make_map_u8_sw128(CUtensorMap* m, const void* base, uint64_t rows, uint64_t
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 2-D byte map, no swizzle; box = box_cols bytes x box_rows rows.
-bool make_map_u8(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
-                 uint32_t box_cols, uint32_t box_rows) {
-  EncodeTiledFn enc = get_encoder();
-  if (!enc) return false;
-  cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {cols};
-  cuuint32_t box[2] = {box_cols, box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 // 2-D map of packed e2m1 codes [rows, cols codes], cols/2 bytes per row;
 // box = 128 codes x box_rows rows, each 16 codes widened to a 16-byte slot
 // in shared memory, 128-byte swizzle.

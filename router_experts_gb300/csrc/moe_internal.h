@@ -206,10 +206,6 @@ bool make_map_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t col
 // swizzle, box = 128 bytes x box_rows rows, zero fill out of bounds.
 bool make_map_u8_sw128(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
                        uint32_t box_rows);
-// 2-D byte map of a row-major [rows, cols] byte matrix, no swizzle, box =
-// box_cols bytes x box_rows rows, zero fill out of bounds.
-bool make_map_u8(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
-                 uint32_t box_cols, uint32_t box_rows);
 // 2-D map of a row-major [rows, cols] matrix of e2m1 codes packed two per
 // byte (low nibble first): each 16 codes land in shared memory as their 8
 // packed bytes followed by an 8-byte gap that the copy leaves untouched (the
