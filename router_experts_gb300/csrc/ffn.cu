@@ -979,8 +979,10 @@ int launch_pair(const CUtensorMap& tw, const CUtensorMap& tin, const FfnParams& 
   return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 
-// GEMM1 row tiles gather with four warps up to this H, with two above it
-// (measured per shape on GB300).
+// GEMM1 row tiles gather with four warps; up to this H one CTA runs a tile,
+// above it CTA pairs do (with four warps each), and the single-CTA kernel
+// that remains above it (task lists past kPairMaxBlocks) keeps two (measured
+// per shape on GB300).
 constexpr int kGather4MaxH = 4096;
 
 int ffn_max_slots(int block_m) { return block_m == 16 ? 1024 : (block_m == 64 ? 256 : 0); }
@@ -1023,7 +1025,7 @@ int launch_ffn_gemm(int kind, int block_m, const void* w, const FfnParams& p, in
     if (block_m == 16) rc = launch_kind<0, 16>(tw, tin, p, num_sms, stream);
     else if (block_m == 64) rc = launch_kind<0, 64>(tw, tin, p, num_sms, stream);
     else if (p.H <= kGather4MaxH) rc = launch_kind<0, 128, 4>(tw, tin, p, num_sms, stream);
-    else if (pair) rc = launch_pair<0, 2>(tw, tin, p, num_sms, stream, why);
+    else if (pair) rc = launch_pair<0, 4>(tw, tin, p, num_sms, stream, why);
     else rc = launch_kind<0, 128>(tw, tin, p, num_sms, stream);
   } else {
     if (block_m == 16) rc = launch_kind<1, 16>(tw, tin, p, num_sms, stream);
