@@ -604,7 +604,7 @@ def kernel_name(w, stage, BM, H):
         if w.lowbit:
             return "lowbit_gemm_kernel<%d>" % kind
         if BM == 128 and H > 4096:  # 128-row tiles on CTA pairs above H = 4096
-            return "ffn_pair_kernel<%d,2>" % kind
+            return "ffn_pair_kernel<%d,%d>" % (kind, 4 if kind == 0 else 2)
         return "ffn_gemm_kernel<%d,%d,%d>" % ((0, BM, gw1) if kind == 0 else (1, BM, 2))
     return {"router": "router_gemm_kernel + router_select_kernel", "align": "align_kernel",
             "finalize": "finalize_kernel"}[stage]
