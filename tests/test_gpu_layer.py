@@ -179,3 +179,26 @@ def test_layer_refuses_strided_tensors():
     xt = d["hidden"].reshape(w.H, 64).t()  # [64, H] view, not contiguous
     with pytest.raises(ValueError, match="contiguous"):
         moe.layer(xt, d["gate"], None, d["w13"], d["w2"], w.k)
+
+
+def test_layer_workspace_reused_across_shapes():
+    # One workspace through calls of several shapes (16-, 64- and one-token
+    # blocks): the layout of each call puts its regions where earlier calls
+    # left other data, and whatever must start at zero lives in the header
+    # or is reset by its last user, so every call still gives the separate
+    # calls' bits.
+    w = W.WORKLOADS["qwen3"]
+    ws = moe.Workspace("cuda")
+    for T in (300, 64, 7, 33, 1, 64):
+        d = W.make_inputs(w, T, seed=T, device="cuda")
+        y = moe.layer(d["hidden"], d["gate"], d.get("bias"), d["w13"], d["w2"], w.k, w.scoring,
+                      ws=ws)
+        ids, wts = moe.router(d["hidden"], d["gate"], d.get("bias"), w.k, w.scoring)
+        bm = moe.pick_block_m(T, w.k, w.E)
+        s, b, n = moe.align(ids, w.E, bm)
+        st = moe.grouped_ffn(d["hidden"], d["w13"], d["w2"], w.k, bm, s, b, n, wts)
+        y2 = moe.finalize(st, T, w.k)
+        torch.cuda.synchronize()
+        print(f"layer qwen3 T={T} (BLOCK_M {bm}) on a reused workspace: equal to the separate calls")
+        assert torch.equal(y, y2)
+        assert moe.read_device_error(ws.buf) == 0
