@@ -552,10 +552,14 @@ struct PairCfg {
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
 
-// The task list, identical in every CTA: paired tasks (blocks b, b+1 of one
-// expert) in block order, then the solo blocks two per task (the second slot
-// kNoBlock when their number is odd).  All threads; scratch: nblk ints of
-// shared memory the ring lends before its first load.
+// The task list, identical in every CTA, in block order: paired tasks
+// (blocks b, b+1 of one expert) and the solo blocks (the odd last block of
+// an expert) two per task (the second slot kNoBlock when their number is
+// odd), a solo task placed where its first block is -- so an expert's last
+// block runs next to its pairs and finds its weight tiles in L2 (queued
+// after all pairs, it fetched them again: DeepSeek-V3 layer T = 4096
+// 3,694 -> 3,446 us).  All threads; scratch: nblk + 2,112 ints of shared
+// memory the ring lends before its first load.
 template <int NTHREADS>
 MOE_DEV int build_pair_tasks(const int32_t* block_expert, int nblk, uint16_t* tb0, uint16_t* tb1,
                              uint8_t* tpair, int* scratch) {
@@ -602,7 +606,39 @@ MOE_DEV int build_pair_tasks(const int32_t* block_expert, int nblk, uint16_t* tb
   __syncthreads();
   const int total = wsum[NW - 1];
   const int NP = total & 0xFFFF, NS = total >> 16;
-  int before = incl - mine + (warp > 0 ? wsum[warp - 1] : 0);
+  const int before0 = incl - mine + (warp > 0 ? wsum[warp - 1] : 0);
+  // tasks in block order: a paired task where its first block is, a solo
+  // task where the first of its two solo blocks is; solo_pos[j]: the task
+  // of solo pair j, which its second block joins after the barrier
+  int* solo_pos = wsum + 64;
+  int before = before0;
+  for (int b = b0; b < b1; ++b) {
+    const int e = be[b];
+    int st = b;
+    while (st > 0 && be[st - 1] == e) --st;
+    int en = b;
+    while (en + 1 < nblk && be[en + 1] == e) ++en;
+    const int L = en - st + 1, j = b - st;
+    const int np = before & 0xFFFF, ns = before >> 16;
+    if ((j & 1) == 0 && j + 1 < L) {
+      const int t = np + (ns + 1) / 2;
+      tb0[t] = static_cast<uint16_t>(b);
+      tb1[t] = static_cast<uint16_t>(b + 1);
+      tpair[t] = 1;
+      before += 1;
+    } else if ((L & 1) && j == L - 1) {
+      if ((ns & 1) == 0) {
+        const int t = np + ns / 2;
+        tb0[t] = static_cast<uint16_t>(b);
+        tb1[t] = kNoBlock;
+        tpair[t] = 0;
+        solo_pos[ns / 2] = t;
+      }
+      before += 1 << 16;
+    }
+  }
+  __syncthreads();
+  before = before0;
   for (int b = b0; b < b1; ++b) {
     const int e = be[b];
     int st = b;
@@ -611,21 +647,10 @@ MOE_DEV int build_pair_tasks(const int32_t* block_expert, int nblk, uint16_t* tb
     while (en + 1 < nblk && be[en + 1] == e) ++en;
     const int L = en - st + 1, j = b - st;
     if ((j & 1) == 0 && j + 1 < L) {
-      const int t = before & 0xFFFF;
-      tb0[t] = static_cast<uint16_t>(b);
-      tb1[t] = static_cast<uint16_t>(b + 1);
-      tpair[t] = 1;
       before += 1;
     } else if ((L & 1) && j == L - 1) {
-      const int is = before >> 16;
-      const int t = NP + is / 2;
-      if ((is & 1) == 0) {
-        tb0[t] = static_cast<uint16_t>(b);
-        if (is == NS - 1) tb1[t] = kNoBlock;
-      } else {
-        tb1[t] = static_cast<uint16_t>(b);
-      }
-      tpair[t] = 0;
+      const int ns = before >> 16;
+      if (ns & 1) tb1[solo_pos[ns / 2]] = static_cast<uint16_t>(b);
       before += 1 << 16;
     }
   }
