@@ -713,10 +713,28 @@ __global__ void __launch_bounds__(Cfg<KIND, 128, GW>::THREADS, 1)
     int b, n, e, eb;
     bool paired;
   };
+  auto task_expert = [&](int t) { return __ldg(p.block_expert + tb0[t]); };
   auto unit_of = [&](int uu) {
     PU x;
-    const int t = uu / ntiles;
+    int t = uu / ntiles;
     x.n = uu % ntiles;
+    if (tpair[t]) {
+      // a run of paired tasks of one expert walks its output tiles n-major:
+      // the clusters on the run share each weight tile at about the same
+      // time (fetched about once instead of once per wave of the run), while
+      // the run's token rows stay in L2 across its output tiles (DeepSeek-V3
+      // layer T = 4096 3,485 -> 3,420 us)
+      const int e0 = task_expert(t);
+      int t0 = t, t1 = t + 1;
+      while (t0 > 0 && tpair[t0 - 1] && task_expert(t0 - 1) == e0) --t0;
+      while (t1 < ntasks && tpair[t1] && task_expert(t1) == e0) ++t1;
+      const int L = t1 - t0;
+      if (L > 1) {
+        const int v = uu - t0 * ntiles;
+        x.n = v / L;
+        t = t0 + v % L;
+      }
+    }
     x.paired = tpair[t] != 0;
     const uint16_t bb = rank == 0 ? tb0[t] : tb1[t];
     x.b = bb == kNoBlock ? -1 : static_cast<int>(bb);
