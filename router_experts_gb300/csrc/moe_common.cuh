@@ -346,7 +346,6 @@ MOE_DEV float ord2f(uint32_t o) {
 // ---------------------------------------------------------------------------
 // small numeric helpers
 // ---------------------------------------------------------------------------
-MOE_DEV float silu_f(float z) { return z / (1.0f + __expf(-z)); }
 // silu(g) * u with silu(g) = g * sigmoid(g) = (g/2) * (1 + tanh(g/2)): one
 // hardware tanh instead of an exponential and a reciprocal.  Relative error
 // about 2^-11, below the bf16 rounding of the result.
